@@ -1,0 +1,477 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 HSDP fully_shard data path.
+
+One step = one pass of the whole hot path over one HSDP unit (all rank_size
+virtual ranks on this GPU): all-gather copy-in fused with the all-gather,
+all-gather copy-out, the fused ReduceScatter + AllReduce gradient sync, and
+applying the averaged gradients to the actual shards. Default workload: the
+large HSDP (2,8) mesh, one 70B-class GQA decoder layer (rank_size 16,
+shard_size 8, 855,654,400 bf16 elements per rank).
+
+Metric: achieved HBM GB/s = algorithmic bytes (what the method must read and
+write; padding that must be written counts, padding that need not be read
+does not) / device time. ``value`` is the whole step; ``kernels`` breaks it
+down; ``roofline`` is the dominant kernel against the measured HBM peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+With N > 1 (torchrun), every GPU runs its own independent unit (weak
+scaling, no data-path collective); rank 0 prints the line with the max time
+over ranks. ``--impl reference`` times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+KERNELS = ["ag_copy_in", "ag_copy_out", "rs_ar_reduce", "apply_grads"]
+METRIC = "achieved HBM GB/s (and % of GB300 peak) for fused RS+AR grad-sync and AG copy-out"
+L2_BYTES = 129 * 1024 * 1024
+ES = {"f32": 4, "bf16": 2}
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="large_hsdp")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# Distributed helpers (one process per GPU; gloo works for CPU tests)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def dist_max(value, world, device="cpu"):
+    """Max of a float over all ranks (the slowest rank sets the time)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(value, world, device="cpu"):
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# Bytes the method must move, per launch
+# --------------------------------------------------------------------------
+
+def algorithmic_bytes(sizes, param_dt, ag_dt, grad_dt):
+    """sizes: dict with W, S, N (elements per rank), shard_total (sum over
+    ranks and params of actual shard elements), slice_ag, slice_f32."""
+    W, S, N = sizes["W"], sizes["S"], sizes["N"]
+    st = sizes["shard_total"]
+    bp, ba, bg = ES[param_dt], ES[ag_dt], ES[grad_dt]
+    return {
+        # read every rank's actual shards; write each rank's slice (data,
+        # padding, tail) into all S shard-group members' buffers
+        "ag_copy_in": st * bp + W * S * sizes["slice_ag"] * ba,
+        # read and write every rank's full parameters (padding not read)
+        "ag_copy_out": 2 * W * N * ba,
+        # read every rank's full gradients once; write every rank's fused region
+        "rs_ar_reduce": W * N * bg + W * sizes["slice_f32"] * 4,
+        # read the actual fused elements; write the actual-shard gradients
+        "apply_grads": st * 4 + st * bg,
+    }
+
+
+def plan_sizes(plan):
+    W, S, P = plan.W, plan.S, plan.P
+    N = sum(plan.numel(p) for p in range(P))
+    st = sum(plan.shard_numel(p, w % S) for w in range(W) for p in range(P))
+    return {"W": W, "S": S, "N": N, "shard_total": st}
+
+
+# --------------------------------------------------------------------------
+# Clocks during the timed region
+# --------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(CLOCK_FIELDS):
+                rows.append(parts)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[0]) for r in rows]
+        power = [num(r[2]) for r in rows]
+        # samples under load: power above the midpoint of the observed range
+        lo, hi = min(power), max(power)
+        loaded = [s for s, p in zip(sm, power) if p >= lo + 0.5 * (hi - lo)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(num(r[1]) for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": hi}
+
+
+# --------------------------------------------------------------------------
+# Oracle on the host: the CPU baseline and the reference arm
+# --------------------------------------------------------------------------
+
+def scaled_workload(wl, f):
+    """The same mesh and parameter list with every dim 0 scaled by f."""
+    d0 = [max(1, int(math.ceil(a * f))) for a in wl.d0]
+    return d0, wl.inner
+
+
+def oracle_step(L, wl, shards, grads):
+    import oracle as O
+
+    pdt, gdt = wl.param_dtype, wl.grad_dtype
+    ag = O.ag_gather(L, O.ag_copy_in(L, shards, pdt, pdt), pdt)
+    O.ag_copy_out(L, ag, pdt)
+    fused = O.fused_from_grads(L, grads, gdt)
+    O.apply_grads(L, fused, "avg", gdt)
+
+
+def oracle_problem(wl, f):
+    import oracle as O
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+
+    d0, inner = scaled_workload(wl, f)
+    L = O.Layout(d0, inner, wl.rank_size, wl.shard_size)
+    shard_sizes = [L.shard_numel(p, w % L.S) for w in range(L.W) for p in range(L.P)]
+    grad_sizes = [L.numel(p) for _ in range(L.W) for p in range(L.P)]
+    shards = WL.np_tensors(shard_sizes, wl.seed_params, wl.param_std, wl.param_dtype)
+    grads = WL.np_tensors(grad_sizes, wl.seed_grads, wl.grad_std, wl.grad_dtype)
+    sizes = {"W": L.W, "S": L.S, "N": sum(grad_sizes) // L.W, "shard_total": sum(shard_sizes),
+             "slice_ag": L.slice(wl.param_dtype), "slice_f32": L.slice("f32")}
+    nbytes = sum(algorithmic_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype).values())
+    return L, shards, grads, nbytes, d0
+
+
+def oracle_calibrate(wl, target_s):
+    """Scale factor of the workload's dim 0 so one oracle step on the host
+    takes about target_s seconds."""
+    f = min(1.0, 2e5 / max(1, wl.numel_per_rank))
+    L, shards, grads, nbytes, _ = oracle_problem(wl, f)
+    t0 = time.perf_counter()
+    oracle_step(L, wl, shards, grads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    return min(1.0, f * target_s / dt)
+
+
+def cpu_baseline(wl, target_s):
+    f = oracle_calibrate(wl, target_s)
+    L, shards, grads, nbytes, d0 = oracle_problem(wl, f)
+    t0 = time.perf_counter()
+    oracle_step(L, wl, shards, grads)
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": (f"one full step (copy-in, gather, copy-out, RS copy-in + fused RS/AR sum, "
+                       f"apply AVG) of the oracle on the same mesh and parameter list with every "
+                       f"dim 0 scaled by {f:.3g} ({sum(a * b for a, b in zip(d0, wl.inner))} "
+                       f"elements per rank, {nbytes / 1e9:.3f} GB algorithmic), single thread")}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist_init(world, "gloo")
+        barrier(world)
+        if rank != 0:
+            return 0
+    per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))
+    f = oracle_calibrate(wl, per_step)
+    L, shards, grads, nbytes, d0 = oracle_problem(wl, f)
+    for _ in range(args.warmup):
+        oracle_step(L, wl, shards, grads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(L, wl, shards, grads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = nbytes / dt / 1e9
+    sample = (f"each step: the oracle's full step on the same mesh and parameter list with every "
+              f"dim 0 scaled by {f:.3g} ({sum(a * b for a, b in zip(d0, wl.inner))} elements per "
+              f"rank), single thread on the host")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.grad_dtype, "data": "synthetic",
+            "config": {"workload": wl.key, "rank_size": wl.rank_size, "shard_size": wl.shard_size,
+                       "elements_per_rank": wl.numel_per_rank, "sampled": True},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# The GPU arm
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return 6800.0, "fallback (6.8 TB/s)"
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same source hash), else None."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "hsdp_sharded_parameter_gb300", "csrc", "fsdp_kernels.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and not line.startswith("#") and parts[0] == h and parts[1] == kernel \
+                and parts[2] == workload:
+            return float(parts[3])
+    return None
+
+
+def run_gpu(args, wl):
+    import torch
+
+    from hsdp_sharded_parameter_gb300 import capi as C
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+    from hsdp_sharded_parameter_gb300.runtime import HsdpUnit
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+
+    plan = C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).upload()
+    unit = HsdpUnit(plan, wl.param_dtype, wl.grad_dtype, device=dev)
+    WL.torch_fill_(unit.shards, wl.seed_params, wl.param_std, wl.param_dtype)
+    WL.torch_fill_(unit.grads, wl.seed_grads, wl.grad_std, wl.grad_dtype)
+    sizes = plan_sizes(plan)
+    sizes["slice_ag"] = plan.slice_numel(wl.param_dtype)
+    sizes["slice_f32"] = plan.slice_numel("f32")
+    kb = algorithmic_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype)
+    step_bytes = sum(kb.values())
+    working_set = step_bytes  # every byte of the step is a distinct HBM location
+    flush = working_set < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    calls = [lambda: unit.ag_copy_in(fuse_gather=True), unit.ag_copy_out, unit.rs_ar_reduce,
+             lambda: unit.apply_grads("avg")]
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        for c in calls:
+            c()
+        if flush:
+            scratch.zero_()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = C.fsdp_launch_count()
+    t_start.record(stream)
+    for k in range(K):
+        if flush:
+            scratch.zero_()
+        ev[k][0].record(stream)
+        for i, c in enumerate(calls):
+            c()
+            ev[k][i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = C.fsdp_launch_count() - l0
+    clk = clocks.stop()
+
+    per_kernel = {n: [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)] for i, n in enumerate(KERNELS)}
+    step_ms = [ev[k][0].elapsed_time(ev[k][len(calls)]) for k in range(K)]
+    total_ms = t_start.elapsed_time(t_end) if not flush else sum(step_ms)
+    my_ms = total_ms / K
+    ms = dist_max(my_ms, world, dev)
+    value = dist_sum(step_bytes, world, dev) / (ms * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    kernels = {}
+    for n in KERNELS:
+        avg = sum(per_kernel[n]) / K
+        gbs = kb[n] / (avg * 1e-3) / 1e9
+        kernels[n] = {"us": round(avg * 1e3, 2), "median_us": round(statistics.median(per_kernel[n]) * 1e3, 2),
+                      "bytes": kb[n], "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    dom = max(KERNELS, key=lambda n: kernels[n]["us"])
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": ncu_traffic(dom, wl.key),
+                "peak_source": peak_src}
+    second = "rs_ar_reduce" if dom != "rs_ar_reduce" else "ag_copy_out"
+    roofline_2 = {"bound": "hbm", "kernel": second, "achieved": kernels[second]["gbs"], "peak": peak,
+                  "unit": "GB/s", "frac": kernels[second]["frac"], "traffic": ncu_traffic(second, wl.key)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, unit, calls, step_bytes, world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": wl.grad_dtype, "data": "synthetic",
+                "config": {"workload": wl.key, "rank_size": wl.rank_size, "shard_size": wl.shard_size,
+                           "dp_size": plan.D, "params": wl.n_params, "elements_per_rank": sizes["N"],
+                           "step_bytes": step_bytes,
+                           "l2": ("flushed between steps (2x L2 scratch write, outside the step events)"
+                                  if flush else "inputs larger than L2 (working set "
+                                  f"{working_set / 1e9:.1f} GB >> 129 MB)"),
+                           "parallelism": f"{world} independent unit(s), one per GPU"},
+                "kernels": kernels, "roofline": roofline, "roofline_second": roofline_2,
+                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches}
+        print(json.dumps(line), flush=True)
+    unit.close()
+    return 0
+
+
+def run_e2e(args, unit, calls, step_bytes, world, dev):
+    """The same metric end to end: every step copies its inputs (the local
+    shards and the full gradients of every rank) from pinned host memory,
+    runs the step, and copies its results (the full parameters and the
+    averaged shard gradients) back to pinned host memory."""
+    import torch
+
+    ins = unit.shards + unit.grads
+    outs = unit.full + unit.shard_grads
+    h_in = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True) for t in ins]
+    h_out = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True) for t in outs]
+    for h, t in zip(h_in, ins):
+        h.copy_(t)
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def one():
+        for t, h in zip(ins, h_in):
+            t.copy_(h, non_blocking=True)
+        for c in calls:
+            c()
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt = dist_max(dt, world, dev)
+    value = dist_sum(step_bytes, world, dev) / dt / 1e9
+    del h_in, h_out
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 2), "steps": args.e2e_steps}
+
+
+def main(argv=None):
+    args = parse(argv)
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+
+    wl = WL.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,247 @@
+"""Thin Python binding of the C-ABI library (include/hsdp_fsdp.h).
+
+Argument marshalling only: every step of the data path runs in the
+library's CUDA kernels. Functions keep the C names; ``Plan`` and
+``Binding`` own the C handles. Tensors are passed as device pointers
+(``data_ptr()``); streams as ``torch.cuda.Stream`` or raw handles.
+
+The library must have been built (``python -m hsdp_sharded_parameter_gb300.build``
+or ``__graft_entry__.build()``): there is no fallback of any kind, a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from .build import library_path
+
+FSDP_OK, FSDP_ERR_INVALID_ARG, FSDP_ERR_NOT_IMPLEMENTED, FSDP_ERR_CUDA, FSDP_ERR_NOMEM = range(5)
+FSDP_F32, FSDP_BF16 = 0, 1
+FSDP_AVG, FSDP_SUM = 0, 1
+(FSDP_ROLE_SHARDS, FSDP_ROLE_AG_OUTPUT, FSDP_ROLE_FULL_PARAMS, FSDP_ROLE_GRADS,
+ FSDP_ROLE_RS_INPUT, FSDP_ROLE_FUSED, FSDP_ROLE_SHARD_GRADS) = range(7)
+
+ROLES = {"shards": FSDP_ROLE_SHARDS, "ag_output": FSDP_ROLE_AG_OUTPUT,
+         "full_params": FSDP_ROLE_FULL_PARAMS, "grads": FSDP_ROLE_GRADS,
+         "rs_input": FSDP_ROLE_RS_INPUT, "fused": FSDP_ROLE_FUSED,
+         "shard_grads": FSDP_ROLE_SHARD_GRADS}
+DTYPES = {"f32": FSDP_F32, "bf16": FSDP_BF16}
+OPS = {"avg": FSDP_AVG, "sum": FSDP_SUM}
+
+_lib = None
+
+
+class FsdpError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"[status {code}] {msg}")
+        self.code = code
+
+
+def header_symbols():
+    """Names of the functions include/hsdp_fsdp.h declares."""
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                       "hsdp_fsdp.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fsdp_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib():
+    """The loaded C-ABI library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing "
+                               "(run __graft_entry__.build())")
+        L = ctypes.CDLL(path)
+        i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+        P = ctypes.POINTER
+        L.fsdp_last_error.restype = ctypes.c_char_p
+        L.fsdp_launch_count.restype = ctypes.c_uint64
+        L.fsdp_plan_create.argtypes = [i32, vp, vp, i32, i32, i32, i32, P(vp)]
+        L.fsdp_plan_destroy.argtypes = [vp]
+        L.fsdp_plan_upload.argtypes = [vp]
+        L.fsdp_plan_info.argtypes = [vp, P(i32), P(i32), P(i32), P(i32), P(i64)]
+        L.fsdp_slice_numel.argtypes = [vp, i32, P(i64)]
+        L.fsdp_sharded_size.argtypes = [vp, i32, i32, P(i64), P(i64)]
+        L.fsdp_padded_sharded_param_size.argtypes = [vp, i32, P(i64)]
+        L.fsdp_offsets.argtypes = [vp, vp]
+        L.fsdp_group_ranks.argtypes = [vp, i32, vp, vp]
+        L.fsdp_comm_calls.argtypes = [vp, P(i32), P(i32)]
+        L.fsdp_bind.argtypes = [vp, i32, i32, vp, vp, P(vp)]
+        L.fsdp_binding_destroy.argtypes = [vp]
+        L.fsdp_ag_copy_in.argtypes = [vp, vp, vp, i32, vp]
+        L.fsdp_ag_gather.argtypes = [vp, vp, vp]
+        L.fsdp_ag_copy_out.argtypes = [vp, vp, vp, vp]
+        L.fsdp_rs_copy_in.argtypes = [vp, vp, vp, vp]
+        L.fsdp_rs_ar_reduce.argtypes = [vp, vp, vp, vp]
+        L.fsdp_apply_grads.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.fsdp_rs_reduce.argtypes = [vp, vp, i32, vp, vp]
+        L.fsdp_ar_reduce.argtypes = [vp, vp, i32, vp]
+        _lib = L
+    return _lib
+
+
+def _check(code):
+    if code != FSDP_OK:
+        raise FsdpError(code, lib().fsdp_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            return 0
+    return getattr(stream, "cuda_stream", stream)
+
+
+def fsdp_launch_count():
+    return int(lib().fsdp_launch_count())
+
+
+class Plan:
+    """Owns an fsdp_plan_t. Host-only until ``upload()``."""
+
+    def __init__(self, dim0, inner, rank_size, shard_size, enable_param_shard=1, shard_dim=0):
+        import numpy as np
+
+        self._d0 = np.ascontiguousarray(dim0, dtype=np.int64)
+        self._inner = np.ascontiguousarray(inner, dtype=np.int64)
+        h = ctypes.c_void_p()
+        _check(lib().fsdp_plan_create(len(self._d0), self._d0.ctypes.data, self._inner.ctypes.data,
+                                      rank_size, shard_size, enable_param_shard, shard_dim,
+                                      ctypes.byref(h)))
+        self.handle = h
+        W, S, D, P = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        sp = ctypes.c_int64()
+        _check(lib().fsdp_plan_info(h, ctypes.byref(W), ctypes.byref(S), ctypes.byref(D),
+                                    ctypes.byref(P), ctypes.byref(sp)))
+        self.W, self.S, self.D, self.P, self.sum_padded = W.value, S.value, D.value, P.value, sp.value
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().fsdp_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def upload(self):
+        _check(lib().fsdp_plan_upload(self.handle))
+        return self
+
+    def slice_numel(self, dt):
+        out = ctypes.c_int64()
+        _check(lib().fsdp_slice_numel(self.handle, DTYPES.get(dt, dt), ctypes.byref(out)))
+        return out.value
+
+    def sharded_size(self, p, s):
+        a, n = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().fsdp_sharded_size(self.handle, p, s, ctypes.byref(a), ctypes.byref(n)))
+        return a.value, n.value
+
+    def padded_sharded_param_size(self, p):
+        c = ctypes.c_int64()
+        _check(lib().fsdp_padded_sharded_param_size(self.handle, p, ctypes.byref(c)))
+        return c.value
+
+    def offsets(self):
+        import numpy as np
+
+        o = np.zeros(self.P + 1, np.int64)
+        _check(lib().fsdp_offsets(self.handle, o.ctypes.data))
+        return o
+
+    def group_ranks(self, w):
+        import numpy as np
+
+        sg = np.zeros(self.S, np.int32)
+        rg = np.zeros(self.D, np.int32)
+        _check(lib().fsdp_group_ranks(self.handle, w, sg.ctypes.data, rg.ctypes.data))
+        return sg, rg
+
+    def comm_calls(self):
+        rs, ar = ctypes.c_int(), ctypes.c_int()
+        _check(lib().fsdp_comm_calls(self.handle, ctypes.byref(rs), ctypes.byref(ar)))
+        return rs.value, ar.value
+
+    # sizes the caller allocates
+    def shard_numel(self, p, s):
+        _, n = self.sharded_size(p, s)
+        return n * int(self._inner[p])
+
+    def numel(self, p):
+        return int(self._d0[p] * self._inner[p])
+
+    def bind(self, role, dt, tensors, check_sizes=True):
+        return Binding(self, role, dt, tensors, check_sizes)
+
+
+class Binding:
+    """Owns an fsdp_binding_t: a device table of the tensors' pointers.
+    Keeps the tensors alive while the binding lives."""
+
+    def __init__(self, plan, role, dt, tensors, check_sizes=True):
+        n = len(tensors)
+        ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in tensors])
+        numels = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in tensors])
+        h = ctypes.c_void_p()
+        _check(lib().fsdp_bind(plan.handle, ROLES.get(role, role), DTYPES.get(dt, dt), ptrs,
+                               numels if check_sizes else None, ctypes.byref(h)))
+        self.handle = h
+        self.plan = plan
+        self.tensors = list(tensors)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().fsdp_binding_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fsdp_ag_copy_in(plan, shards, ag_out, fuse_gather=False, stream=None):
+    _check(lib().fsdp_ag_copy_in(plan.handle, shards.handle, ag_out.handle, int(bool(fuse_gather)),
+                                 _stream(stream)))
+
+
+def fsdp_ag_gather(plan, ag_out, stream=None):
+    _check(lib().fsdp_ag_gather(plan.handle, ag_out.handle, _stream(stream)))
+
+
+def fsdp_ag_copy_out(plan, ag_out, full_params, stream=None):
+    _check(lib().fsdp_ag_copy_out(plan.handle, ag_out.handle, full_params.handle, _stream(stream)))
+
+
+def fsdp_rs_copy_in(plan, grads, rs_in, stream=None):
+    _check(lib().fsdp_rs_copy_in(plan.handle, grads.handle, rs_in.handle, _stream(stream)))
+
+
+def fsdp_rs_ar_reduce(plan, grads, fused, stream=None):
+    _check(lib().fsdp_rs_ar_reduce(plan.handle, grads.handle, fused.handle, _stream(stream)))
+
+
+def fsdp_apply_grads(plan, fused, op, shard_grads, accumulate=False, stream=None):
+    _check(lib().fsdp_apply_grads(plan.handle, fused.handle, OPS.get(op, op), int(bool(accumulate)),
+                                  shard_grads.handle, _stream(stream)))
+
+
+def fsdp_rs_reduce(plan, rs_in, op, fused, stream=None):
+    _check(lib().fsdp_rs_reduce(plan.handle, rs_in.handle, OPS.get(op, op), fused.handle,
+                                _stream(stream)))
+
+
+def fsdp_ar_reduce(plan, fused, op, stream=None):
+    _check(lib().fsdp_ar_reduce(plan.handle, fused.handle, OPS.get(op, op), _stream(stream)))

@@ -1,0 +1,132 @@
+// Internal definitions shared by the host plan code, the C-ABI entry points
+// and the kernels of the GB300 HSDP data path. Not installed; the public
+// interface is include/hsdp_fsdp.h.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "hsdp_fsdp.h"
+
+namespace fsdp {
+
+// One contiguous run of work: n elements written at dst_off of the
+// destination buffer(s), read from src_off of the source buffer(s). p < 0
+// marks a run of zeros (padding rows, slice tails). `row` is the shard rank
+// s the run belongs to; how src/dst buffers are picked from (row, p, rep)
+// depends on the kernel.
+struct Seg {
+    int64_t n;
+    int64_t dst_off;
+    int64_t src_off;
+    int32_t p;
+    int32_t row;
+};
+static_assert(sizeof(Seg) == 32, "Seg is 32 bytes on host and device");
+
+// Work is cut into warp tiles: 32 lanes x 4 steps x 8 elements. A lane
+// moves 8 consecutive elements per step (16 B of bf16, 32 B of fp32), so a
+// warp step covers 256 consecutive elements. Granules are anchored at
+// 16-byte boundaries of the destination: a run whose first destination
+// element is not 16-byte aligned starts with a partial granule.
+constexpr int kGran = 8;
+constexpr int kSteps = 4;
+constexpr int kWarpTile = 32 * kSteps * kGran;  // 1024 elements
+constexpr int kThreads = 256;
+
+// Work tables. Each kernel walks one: a list of runs plus, per run, the
+// index of its first warp tile (prefix sum, nseg + 1 entries).
+enum TableId {
+    T_RSAR = 0,        // fused RS+AR: rows of the fp32 fused region, per s
+    T_AGIN_F32,        // copy-in: rows of the ag slice, per s (f32 ag dtype)
+    T_AGIN_BF16,       //          (bf16 ag dtype)
+    T_GATHER_F32,      // all-gather: whole slice s, per s
+    T_GATHER_BF16,
+    T_AGOUT_F32,       // copy-out: (p, s) pieces of the full parameters
+    T_AGOUT_BF16,
+    T_RSIN_F32,        // RS copy-in: rows of the RS input, per s
+    T_RSIN_BF16,
+    T_APPLY,           // apply: (s, p) actual-shard pieces of the fused region
+    T_RS_F32,          // unfused RS: row s of an f32 RS input
+    T_RS_BF16,         //             row s of a bf16 RS input
+    T_AR,              // unfused AR: fp32 fused region, per s
+    T_COUNT
+};
+
+struct Table {
+    const Seg* segs = nullptr;           // device
+    const int64_t* tile_begin = nullptr; // device, nseg + 1
+    int nseg = 0;
+    int64_t ntiles = 0;
+};
+
+inline int elem_size(int dt) { return dt == FSDP_F32 ? 4 : (dt == FSDP_BF16 ? 2 : 0); }
+
+// Arguments of every kernel (passed by value).
+struct KArgs {
+    const Seg* segs;
+    const int64_t* tile_begin;
+    int nseg;
+    int64_t ntiles;  // tiles of one repetition
+    int reps;        // repetitions of the table (ranks or replicas)
+    int P, S, D, W;
+    void* const* src_tab;  // device table of source pointers
+    void* const* dst_tab;  // device table of destination pointers
+    int fuse;              // copy-in: also write every shard-group member
+    int vec;               // 1: every destination is 16-byte aligned
+    int op;                // FSDP_AVG / FSDP_SUM
+    int accumulate;        // apply: add to the gradient already there
+    float div;             // divisor applied after the sum (1 = none)
+};
+
+enum Kind {
+    K_AGIN = 0,
+    K_GATHER,
+    K_AGOUT,
+    K_RSIN,
+    K_RSAR,
+    K_RS,
+    K_AR,
+    K_APPLY
+};
+
+// Launches the kernel of `kind` for the given element types. Returns a
+// cudaError_t of the launch.
+cudaError_t launch(Kind kind, int src_dt, int dst_dt, const KArgs& a, cudaStream_t stream);
+
+}  // namespace fsdp
+
+struct fsdp_plan_s {
+    int P = 0, W = 1, S = 1, D = 1;
+    std::vector<int64_t> d0, inner, chunk, off, len, o;  // off/len: [P*S]
+    int64_t sum_padded = 0;
+    int device = -1;
+    bool uploaded = false;
+    void* dev_block = nullptr;
+    fsdp::Table tables[fsdp::T_COUNT];
+    int64_t slice(int dt) const {
+        int64_t per = 512 / fsdp::elem_size(dt);
+        return (sum_padded + per - 1) / per * per;
+    }
+};
+
+struct fsdp_binding_s {
+    fsdp_plan_s* plan = nullptr;
+    int role = -1;
+    int dt = -1;
+    int count = 0;
+    void** dev_table = nullptr;
+    bool aligned16 = true;
+};
+
+namespace fsdp {
+int set_error(int code, const std::string& msg);
+void clear_error();
+void count_launch();
+// Builds the host-side work tables of a plan (used by fsdp_plan_upload).
+void build_tables(const fsdp_plan_s& plan, std::vector<Seg> segs[T_COUNT],
+                  std::vector<int64_t> tiles[T_COUNT]);
+}  // namespace fsdp

@@ -148,23 +148,33 @@ def np_tensors(sizes, seed, std, dtype):
     return [_np_draw(rng, int(n), std, dtype) for n in sizes]
 
 
+def torch_fill_(tensors, seed, std, dtype):
+    """Fill existing flat device tensors in order from one seeded generator
+    on their device: N(0, std^2) drawn in fp32, then stored in the tensors'
+    dtype (bf16 by PyTorch's round-to-nearest conversion)."""
+    import torch
+
+    if not tensors:
+        return tensors
+    gen = torch.Generator(device=tensors[0].device)
+    gen.manual_seed(seed)
+    for t in tensors:
+        n = t.numel()
+        if n:
+            x = torch.randn(n, generator=gen, device=t.device, dtype=torch.float32)
+            t.copy_(x.mul_(std))
+            del x
+    return tensors
+
+
 def torch_tensors(sizes, seed, std, dtype, device):
     """One flat torch tensor per entry of ``sizes``, each a separate
     allocation on ``device``, drawn in order from one seeded generator."""
     import torch
 
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
-    out = []
-    for n in sizes:
-        t = torch.empty(int(n), dtype=tdt, device=device)
-        if n:
-            x = torch.randn(int(n), generator=gen, device=device, dtype=torch.float32)
-            t.copy_(x.mul_(std))
-            del x
-        out.append(t)
-    return out
+    out = [torch.empty(int(n), dtype=tdt, device=device) for n in sizes]
+    return torch_fill_(out, seed, std, dtype)
 
 
 def grad_sizes(wl):

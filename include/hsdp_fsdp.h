@@ -1,0 +1,248 @@
+/*
+ * hsdp_fsdp.h -- C ABI of the GB300 HSDP fully_shard data path with dim-0
+ * ragged (uneven) parameter shards.
+ *
+ * All rank_size = W virtual ranks live in ONE GPU's HBM. Virtual rank w sits
+ * at mesh coordinate (d, s) = (w / S, w % S): d is the replicate index
+ * (0 <= d < D = dp_size), s the shard rank (0 <= s < S = shard_size). The
+ * shard group of w is {d*S + k : k < S} (the ReduceScatter / AllGather
+ * group); its replicate group is {k*S + s : k < D} (the AllReduce group).
+ * The collectives of the pages become kernels that read and write the ranks'
+ * buffers in place; there is no second GPU and no NCCL.
+ *
+ * Sources (page title + section):
+ *   [FS-RFC]  "【RFC】FullyShard 多维并行适配设计方案" (hyper-parallel issue 1)
+ *   [OVERLAP] "Hyper通信掩盖方案" (hyper-parallel issue 184) and its PR #758
+ *             write-up ("方案落地说明")
+ *   [RAGGED]  FSDP dim-0 uneven-sharding RFC (hyper-parallel issue 319)
+ *
+ * Layout (all element offsets, row-major tensors):
+ *   parameter p has shape (d0_p, rest...), inner_p = prod(rest) (1 for a
+ *   vector). chunk_p = ceil(d0_p / S) ("padded_sharded_param_size" rows);
+ *   shard s of p holds rows [off_{p,s}, off_{p,s} + len_{p,s}) with
+ *   off = min(s*chunk, d0), len = min(chunk, d0 - off) ("sharded_size",
+ *   possibly 0) [RAGGED §6.4]. Inside a per-rank slice parameter p starts at
+ *   o_p = sum_{q<p} chunk_q * inner_q and occupies chunk_p * inner_p
+ *   elements; the rows past len are zero. A slice holds slice(dt) elements:
+ *   sum_p chunk_p*inner_p rounded up to a multiple of 512 bytes [OVERLAP
+ *   PR #758 §二.1, the 512B-aligned fused buffer].
+ *
+ * Conventions for every call:
+ *   - Return value: FSDP_OK (0) or an error code; the message of the last
+ *     failure on the calling thread is fsdp_last_error().
+ *   - Memory: the caller allocates and frees every data buffer (PyTorch
+ *     here). The library owns only plans and bindings (small device tables
+ *     allocated by fsdp_plan_upload / fsdp_bind and freed by the matching
+ *     destroy). Data calls never allocate, never free, never synchronise.
+ *   - Streams: data calls enqueue exactly one kernel on `stream` (NULL = the
+ *     legacy default stream) and return; launch failures come back as
+ *     FSDP_ERR_CUDA. Calls on different streams are safe when the buffers
+ *     they write are disjoint from the buffers the others touch.
+ *   - Pointers: device pointers aligned to their element size; NULL only
+ *     for a buffer of 0 elements. 16-byte-aligned pointers (every PyTorch
+ *     allocation) take the vectorised path; others take an element-wise
+ *     path with identical results.
+ *   - Numerics: sums are IEEE binary32 additions, round to nearest even,
+ *     subnormals kept, folded in ascending rank order: first over the shard
+ *     group, then over the replicas. float -> bf16 rounds to nearest even;
+ *     a NaN becomes the quiet NaN 0x7FC0 with its sign.
+ */
+#ifndef HSDP_FSDP_H
+#define HSDP_FSDP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fsdp_plan_s* fsdp_plan_t;
+typedef struct fsdp_binding_s* fsdp_binding_t;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fsdp_stream_t;
+
+enum fsdp_status {
+    FSDP_OK = 0,
+    FSDP_ERR_INVALID_ARG = 1,     /* bad argument, size, dtype or state */
+    FSDP_ERR_NOT_IMPLEMENTED = 2, /* uneven sharding of a dim other than 0 */
+    FSDP_ERR_CUDA = 3,            /* a CUDA runtime call failed */
+    FSDP_ERR_NOMEM = 4            /* host or device allocation failed */
+};
+
+enum fsdp_dtype { FSDP_F32 = 0, FSDP_BF16 = 1 };
+
+/* AVG and SUM as in [OVERLAP] PR #758 §二.3 (_resolve_default_reduce_op:
+ * AVG by default, SUM for DTensor-managed parameters). */
+enum fsdp_reduce_op { FSDP_AVG = 0, FSDP_SUM = 1 };
+
+/* What a binding's pointers are. "[W][P]" tables hold one pointer per
+ * (rank, parameter), index w*P + p; "[W]" tables one pointer per rank.
+ * Required element counts (checked by fsdp_bind when numels is given):
+ *   SHARDS       [W][P] local actual shard of p on rank w:  len_{p,s} * inner_p
+ *   AG_OUTPUT    [W]    all-gather buffer of rank w:        S * slice(dt)
+ *   FULL_PARAMS  [W][P] unsharded parameter p on rank w:    d0_p * inner_p
+ *   GRADS        [W][P] unsharded gradient p on rank w:     d0_p * inner_p
+ *   RS_INPUT     [W]    reduce-scatter input of rank w:     S * slice(dt)
+ *   FUSED        [W]    fused fp32 gradient region of w:    slice(F32)   (F32 only)
+ *   SHARD_GRADS  [W][P] actual-shard gradient p on rank w:  len_{p,s} * inner_p
+ */
+enum fsdp_role {
+    FSDP_ROLE_SHARDS = 0,
+    FSDP_ROLE_AG_OUTPUT = 1,
+    FSDP_ROLE_FULL_PARAMS = 2,
+    FSDP_ROLE_GRADS = 3,
+    FSDP_ROLE_RS_INPUT = 4,
+    FSDP_ROLE_FUSED = 5,
+    FSDP_ROLE_SHARD_GRADS = 6
+};
+
+/* Message of the last failed call on this thread ("" if none). The string
+ * stays valid until the next call on this thread. */
+const char* fsdp_last_error(void);
+
+/* Number of kernels this library has enqueued in this process. */
+uint64_t fsdp_launch_count(void);
+
+/* ---------------------------------------------------------------- plan */
+
+/* Creates a host-only plan for n_params parameters registered in order.
+ * dim0[p] >= 0 is the dim-0 length, inner[p] >= 1 the product of the other
+ * dims (1 for a vector; a 0-dim scalar is passed as dim0 = 1, inner = 1).
+ * rank_size = W >= 1. shard_size = S must divide W; dp_size = W / S
+ * [FS-RFC §2.2.5]. enable_param_shard = 0 switches parameter sharding off
+ * and forces S = 1 (AllReduce only, the pure-TP compatibility path)
+ * [FS-RFC §2.2.3 option A, §4.1]. shard_dim must be 0: uneven sharding of
+ * another dim is a non-goal [RAGGED §3.2] -> FSDP_ERR_NOT_IMPLEMENTED.
+ * Needs no GPU. *out receives a handle owned by the caller. */
+int fsdp_plan_create(int n_params, const int64_t* dim0, const int64_t* inner, int rank_size,
+                     int shard_size, int enable_param_shard, int shard_dim, fsdp_plan_t* out);
+
+/* Frees the plan and its device tables. The caller must ensure no enqueued
+ * work still uses them (e.g. synchronise the streams first). NULL is a no-op. */
+int fsdp_plan_destroy(fsdp_plan_t plan);
+
+/* Uploads the plan's work tables to the current CUDA device (synchronous,
+ * allocates device memory once). Required before any data call; data calls
+ * must then run with that device current. Calling it again is a no-op. */
+int fsdp_plan_upload(fsdp_plan_t plan);
+
+/* Mesh sizes and the unpadded total sum_p chunk_p * inner_p. Any output
+ * pointer may be NULL. */
+int fsdp_plan_info(fsdp_plan_t plan, int* rank_size, int* shard_size, int* dp_size,
+                   int* n_params, int64_t* sum_padded);
+
+/* Elements of one per-rank slice for dtype dt: sum_padded rounded up to a
+ * multiple of 512 bytes [OVERLAP PR #758 §二.1]. */
+int fsdp_slice_numel(fsdp_plan_t plan, int dt, int64_t* out);
+
+/* "sharded_size" of parameter p on shard rank s [RAGGED §6.4]: the first
+ * row and the number of rows it holds (possibly 0). */
+int fsdp_sharded_size(fsdp_plan_t plan, int p, int shard_rank, int64_t* offset_rows,
+                      int64_t* length_rows);
+
+/* "padded_sharded_param_size" of parameter p: chunk_p = ceil(d0_p / S)
+ * rows [RAGGED §6.4]; its numel is chunk_p * inner_p. */
+int fsdp_padded_sharded_param_size(fsdp_plan_t plan, int p, int64_t* chunk_rows);
+
+/* Element offsets o_0 .. o_P of the parameters inside a slice (n_params+1
+ * values; o_P = sum_padded). */
+int fsdp_offsets(fsdp_plan_t plan, int64_t* offsets);
+
+/* Rank lists of rank w: shard_group[S] (ReduceScatter/AllGather group) and
+ * replicate_group[D] (AllReduce group) [FS-RFC §2.2.1]. Either may be NULL. */
+int fsdp_group_ranks(fsdp_plan_t plan, int w, int* shard_group, int* replicate_group);
+
+/* Collectives the gradient sync issues [FS-RFC §2.2.2]: *rs_group_size = S
+ * if a ReduceScatter over the shard group is issued (S > 1), else 0;
+ * *ar_group_size = D if an AllReduce over the replicate group is issued
+ * (D > 1), else 0. */
+int fsdp_comm_calls(fsdp_plan_t plan, int* rs_group_size, int* ar_group_size);
+
+/* ------------------------------------------------------------- bindings */
+
+/* Uploads a pointer table for `role` (see enum fsdp_role) with element type
+ * dt to the plan's device. dev_ptrs: host array of W*P or W device pointers.
+ * numels: optional host array (same length) of the buffers' element counts,
+ * checked against the role's requirement; NULL skips the check and makes
+ * the caller responsible for the sizes. Pointers are checked for element
+ * alignment. The plan must be uploaded. *out receives a handle owned by the
+ * caller; the pointed-to buffers stay owned by the caller. */
+int fsdp_bind(fsdp_plan_t plan, int role, int dt, const void* const* dev_ptrs,
+              const int64_t* numels, fsdp_binding_t* out);
+
+/* Frees a binding's device table (same caveat as fsdp_plan_destroy). */
+int fsdp_binding_destroy(fsdp_binding_t binding);
+
+/* --------------------------------------------------- forward (unshard) */
+
+/* All-gather copy-in [OVERLAP PR #758 §二.1, §四.1; RAGGED §6.4]: rank w =
+ * (d, s) packs its shards (SHARDS, dtype F32 or BF16) into ITS OWN slice of
+ * its all-gather buffer (AG_OUTPUT, elements [s*slice, (s+1)*slice)), cast
+ * F32->F32, F32->BF16 (round to nearest even) or BF16->BF16; padding rows
+ * and the slice tail become 0. With fuse_gather != 0 the same slice is also
+ * written into every shard-group member's buffer at the same place, so the
+ * AllGather needs no separate pass. */
+int fsdp_ag_copy_in(fsdp_plan_t plan, fsdp_binding_t shards, fsdp_binding_t ag_out,
+                    int fuse_gather, fsdp_stream_t stream);
+
+/* The AllGather over each shard group [OVERLAP §四.1]: copies slice s of
+ * rank (d, s) into slice s of every other member (d, s'). */
+int fsdp_ag_gather(fsdp_plan_t plan, fsdp_binding_t ag_out, fsdp_stream_t stream);
+
+/* All-gather copy-out [OVERLAP PR #758 §二.1; RAGGED §6.4]: unpacks each
+ * rank's gathered buffer into its full parameters (FULL_PARAMS, same dtype):
+ * row r of parameter p comes from slice r / chunk_p, local row
+ * r % chunk_p; padding rows are dropped. */
+int fsdp_ag_copy_out(fsdp_plan_t plan, fsdp_binding_t ag_out, fsdp_binding_t full_params,
+                     fsdp_stream_t stream);
+
+/* ------------------------------------------------- backward (grad sync) */
+
+/* Reduce-scatter copy-in [RAGGED §6.4; OVERLAP PR #758 §二.1]: row s' of
+ * rank w's RS input (RS_INPUT, same dtype as GRADS) holds rows
+ * [off_{p,s'}, off+len) of every gradient p at o_p, zeros to the padded
+ * size and in the slice tail. Used by the unfused path. */
+int fsdp_rs_copy_in(fsdp_plan_t plan, fsdp_binding_t grads, fsdp_binding_t rs_in,
+                    fsdp_stream_t stream);
+
+/* Fused gradient sync: reduce-scatter copy-in + ReduceScatter (SUM over the
+ * shard group) + AllReduce (SUM over the replicate group) into the fused
+ * fp32 regions, in one pass that reads every unpadded gradient once
+ * [OVERLAP PR #758 §二.1 AllReduceParamGroup zero-copy fused buffer, §二.3
+ * fused AllReduce uses SUM]. For rank (d, s) and element j < slice(F32):
+ * fused_{d,s}[j] = sum_{d'} sum_{s''} grads_{(d',s''),p}[off_{p,s}*inner_p +
+ * j - o_p] when j lies in the actual rows of parameter p's region, +0
+ * otherwise. GRADS: F32 or BF16; FUSED: F32. No scaling happens here. */
+int fsdp_rs_ar_reduce(fsdp_plan_t plan, fsdp_binding_t grads, fsdp_binding_t fused,
+                      fsdp_stream_t stream);
+
+/* Applies synced gradients [OVERLAP PR #758 §二.3 wait_and_apply_grads;
+ * RAGGED §6.4 back-fill by sharded_size]: for rank (d, s) and parameter p,
+ * shard_grads[k] = round(fused[o_p + k] / div) for k < len_{p,s}*inner_p,
+ * div = W for FSDP_AVG (the fused buffer holds the SUM over all W ranks),
+ * 1 for FSDP_SUM. With accumulate != 0 the result is added, in fp32, to the
+ * gradient already in shard_grads and rounded once (grad accumulation,
+ * [FS-RFC §5.2 item 9]). SHARD_GRADS: F32 or BF16. Zero-length shards are
+ * not touched. */
+int fsdp_apply_grads(fsdp_plan_t plan, fsdp_binding_t fused, int op, int accumulate,
+                     fsdp_binding_t shard_grads, fsdp_stream_t stream);
+
+/* Unfused path, ReduceScatter half [OVERLAP PR #758 §二.3-§二.4]: for rank
+ * (d, s), fused[j] = sum_{s''} rs_in_{(d,s'')}[s*slice(dt_in) + j] for
+ * j < slice(F32), divided by S for FSDP_AVG. */
+int fsdp_rs_reduce(fsdp_plan_t plan, fsdp_binding_t rs_in, int op, fsdp_binding_t fused,
+                   fsdp_stream_t stream);
+
+/* Unfused path, AllReduce half, in place over each replicate group
+ * [OVERLAP PR #758 §二.4 fix 1: the replicate-dim AllReduce is scaled by
+ * replicate_world_size]: fused_{(d,s)}[j] = sum_{d'} fused_{(d',s)}[j] for
+ * every d, divided by D for FSDP_AVG. With power-of-two S and D, rs_reduce
+ * (AVG) + ar_reduce (AVG) + apply_grads (SUM) equals rs_ar_reduce +
+ * apply_grads (AVG) bit for bit. */
+int fsdp_ar_reduce(fsdp_plan_t plan, fsdp_binding_t fused, int op, fsdp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSDP_FSDP_H */

@@ -1,0 +1,92 @@
+"""C-ABI host side, no GPU: the library loads, exports every declared symbol,
+and its plan (pure host logic) equals the oracle's plan integer for integer."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from hsdp_sharded_parameter_gb300 import capi as C
+from hsdp_sharded_parameter_gb300 import workloads as WL
+
+
+def test_library_exports_every_declared_symbol():
+    names = C.header_symbols()
+    assert len(names) >= 20
+    lib = C.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert missing == []
+
+
+PLANS = [(4, 1, [7, 16, 5, 3], [8, 8, 1, 4]),
+         (3, 2, [0, 1, 2, 10, 11, 40], [5, 1, 17, 3, 1, 2]),
+         (1, 8, [9, 4], [3, 1]),
+         (8, 2, [1, 2, 3, 4, 5, 6, 7, 8, 9], [1] * 9),
+         (5, 3, list(range(30)), [1 + i % 7 for i in range(30)])]
+
+
+def same_plan(cp, op):
+    assert (cp.W, cp.S, cp.D, cp.P, cp.sum_padded) == (op.W, op.S, op.D, op.P, op.sum_padded)
+    assert np.array_equal(cp.offsets(), op.o)
+    for p in range(op.P):
+        assert cp.padded_sharded_param_size(p) == op.dss[p]
+        for s in range(op.S):
+            assert cp.sharded_size(p, s) == (op.off[p, s], op.len[p, s])
+    for dt in ["f32", "bf16"]:
+        assert cp.slice_numel(dt) == op.slice(dt)
+    for w in range(op.W):
+        a, b = cp.group_ranks(w), op.group_ranks(w)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert cp.comm_calls() == op.comm_calls()
+
+
+@pytest.mark.parametrize("S,D,d0,inner", PLANS)
+def test_plan_equals_oracle(S, D, d0, inner):
+    same_plan(C.Plan(d0, inner, S * D, S), O.Layout(d0, inner, S * D, S))
+
+
+@pytest.mark.parametrize("key", WL.ORDER)
+def test_workload_plans_equal_oracle(key):
+    wl = WL.WORKLOADS[key]
+    same_plan(C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size),
+              O.Layout(wl.d0, wl.inner, wl.rank_size, wl.shard_size))
+
+
+def test_enable_param_shard_off_forces_shard_size_one():
+    cp = C.Plan([8, 3], [4, 1], 8, 4, enable_param_shard=0)
+    assert (cp.S, cp.D) == (1, 8)
+    assert cp.comm_calls() == (0, 8)
+
+
+def test_errors_are_reported_not_crashed():
+    with pytest.raises(C.FsdpError) as e:
+        C.Plan([7], [8], 4, 4, shard_dim=1)
+    assert e.value.code == C.FSDP_ERR_NOT_IMPLEMENTED and "shard_dim" in str(e.value)
+    with pytest.raises(C.FsdpError) as e:
+        C.Plan([7], [8], 6, 4)
+    assert e.value.code == C.FSDP_ERR_INVALID_ARG
+    with pytest.raises(C.FsdpError) as e:
+        C.Plan([7], [0], 4, 4)
+    assert e.value.code == C.FSDP_ERR_INVALID_ARG
+    cp = C.Plan([7], [8], 4, 4)
+    with pytest.raises(C.FsdpError):
+        cp.sharded_size(1, 0)
+    with pytest.raises(C.FsdpError):
+        cp.sharded_size(0, 4)
+    lib = C.lib()
+    assert lib.fsdp_plan_destroy(None) == 0
+    h = ctypes.c_void_p()
+    # a data call on a plan that was never uploaded is refused on the host
+    rc = lib.fsdp_rs_ar_reduce(cp.handle, None, None, None)
+    assert rc == C.FSDP_ERR_INVALID_ARG and b"not uploaded" in lib.fsdp_last_error()
+    rc = lib.fsdp_bind(cp.handle, 0, 0, None, None, ctypes.byref(h))
+    assert rc == C.FSDP_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_upload_without_gpu_fails_cleanly():
+    cp = C.Plan([7], [8], 4, 4)
+    with pytest.raises(C.FsdpError) as e:
+        cp.upload()
+    assert e.value.code in (C.FSDP_ERR_CUDA, C.FSDP_ERR_NOMEM)

@@ -1,0 +1,139 @@
+"""GPU parity on small plans: every output buffer of every C-ABI call equals
+the CPU oracle byte for byte, padding and untouched regions included; guard
+bands around every buffer stay intact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from hsdp_sharded_parameter_gb300 import capi as C
+from hsdp_sharded_parameter_gb300 import workloads as WL
+from hsdp_sharded_parameter_gb300.runtime import HsdpUnit
+
+from gpu_util import GuardedAlloc, check_every_step, make, to_np, fill_
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_workload_every_step():
+    wl = WL.WORKLOADS["tiny_fsdp"]
+    plan, L, unit, alloc = make(4, 1, wl.d0, wl.inner, "f32", "f32")
+    assert check_every_step(L, unit, alloc, seed=wl.seed_params) > 30
+
+
+def test_tiny_workload_with_bf16_gather_cast():
+    # all-gather copy-in with cast f32 -> bf16 ("Hyper通信掩盖方案" PR #758 §二.1)
+    wl = WL.WORKLOADS["tiny_fsdp"]
+    plan, L, unit, alloc = make(4, 1, wl.d0, wl.inner, "f32", "f32", ag_dt="bf16")
+    check_every_step(L, unit, alloc, seed=7)
+
+
+def random_plan(seed):
+    rng = np.random.default_rng(seed)
+    S = int(rng.integers(1, 10))
+    D = int(rng.integers(1, 5))
+    P = int(rng.integers(1, 9))
+    d0 = [int(x) for x in rng.integers(0, 41, P)]
+    inner = [int(x) for x in rng.choice([1, 1, 2, 3, 5, 8, 16, 17, 64], P)]
+    pdt, gdt, adt = [("bf16", "bf16", "bf16"), ("f32", "f32", "f32"), ("f32", "bf16", "bf16"),
+                     ("f32", "f32", "bf16")][int(rng.integers(0, 4))]
+    return S, D, d0, inner, pdt, gdt, adt
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_plans(seed):
+    S, D, d0, inner, pdt, gdt, adt = random_plan(seed)
+    plan, L, unit, alloc = make(S, D, d0, inner, pdt, gdt, adt)
+    check_every_step(L, unit, alloc, seed=seed)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_long_ragged_runs_span_many_tiles(seed):
+    # runs of several warp tiles with ragged heads and tails, shifted sources
+    rng = np.random.default_rng(100 + seed)
+    S = int(rng.integers(2, 9))
+    D = int(rng.integers(1, 3))
+    d0 = [int(x) for x in rng.integers(1, 3000, 5)] + [S - 1, 1]
+    inner = [int(x) for x in rng.choice([1, 3, 7, 128, 33], len(d0))]
+    plan, L, unit, alloc = make(S, D, d0, inner, "bf16", "bf16")
+    check_every_step(L, unit, alloc, seed=seed, ops=("avg",))
+
+
+@pytest.mark.parametrize("offsets", [
+    # sources shifted against 16-byte boundaries, destinations aligned: funnel-shift path
+    {"shards": 2, "grads": 6, "ag_output": 0},
+    # every buffer off 16-byte alignment: element-wise path everywhere
+    {"shards": 2, "grads": 2, "ag_output": 2, "full_params": 4, "fused": 4, "shard_grads": 2,
+     "rs_input": 6},
+])
+def test_unaligned_pointers(offsets):
+    plan, L, unit, alloc = make(4, 2, [13, 40, 7, 1, 300], [5, 1, 16, 3, 9], "bf16", "bf16",
+                                offsets=offsets)
+    check_every_step(L, unit, alloc, seed=3)
+
+
+@pytest.mark.parametrize("dts", [("bf16", "bf16", "bf16"), ("f32", "f32", "f32"), ("f32", "bf16", "bf16")])
+def test_special_values(dts):
+    # subnormals (kept: no flush to zero), signed zeros, overflow to infinity,
+    # Inf - Inf = NaN, rounding ties
+    plan, L, unit, alloc = make(2, 2, [33, 8, 150], [9, 1, 4], *dts)
+    check_every_step(L, unit, alloc, seed=11, special=True)
+
+
+def test_fused_and_unfused_paths_agree_bitwise():
+    # "Hyper通信掩盖方案" PR #758 §二.4 fix 1 / §三: fused and unfused AVG agree.
+    wl = WL.WORKLOADS["hsdp_2x4_llama"]
+    d0 = [a // 64 for a in wl.d0]
+    inner = [max(1, i // 64) for i in wl.inner]
+    plan, L, unit, alloc = make(4, 2, d0, inner, "bf16", "bf16")
+    fill_(unit.grads, 5, 0.02, "bf16")
+    unit.reduce_grads("avg")
+    a = [to_np(t).copy() for t in unit.shard_grads]
+    unit.reduce_grads_unfused("avg")
+    b = [to_np(t) for t in unit.shard_grads]
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_each_call_launches_exactly_one_kernel():
+    plan, L, unit, alloc = make(4, 2, [7, 16], [8, 1], "bf16", "bf16")
+    c0 = C.fsdp_launch_count()
+    unit.step()
+    torch.cuda.synchronize()
+    assert C.fsdp_launch_count() - c0 == 4  # copy-in(+gather), copy-out, rs_ar_reduce, apply
+    c0 = C.fsdp_launch_count()
+    unit.unshard(fuse_gather=False)
+    unit.reduce_grads_unfused()
+    torch.cuda.synchronize()
+    assert C.fsdp_launch_count() - c0 == 7
+
+
+def test_empty_and_degenerate_plans():
+    # all parameters empty: the slices are 0 elements and nothing launches
+    plan = C.Plan([0, 0], [4, 1], 4, 2).upload()
+    assert plan.slice_numel("f32") == 0
+    unit = HsdpUnit(plan, "bf16", "bf16")
+    c0 = C.fsdp_launch_count()
+    unit.step()
+    torch.cuda.synchronize()
+    assert C.fsdp_launch_count() == c0
+    # S = D = 1: no communication, the gradient is kept
+    plan, L, unit, alloc = make(1, 1, [5, 3], [3, 2], "f32", "f32")
+    check_every_step(L, unit, alloc, seed=2)
+
+
+def test_bad_bindings_are_refused():
+    plan = C.Plan([7, 16], [8, 1], 4, 2).upload()
+    ok = [torch.empty(plan.shard_numel(p, w % 2), dtype=torch.bfloat16, device="cuda")
+          for w in range(4) for p in range(2)]
+    with pytest.raises(C.FsdpError) as e:  # too small
+        plan.bind("shards", "bf16", [torch.empty(1, dtype=torch.bfloat16, device="cuda")] * 8)
+    assert e.value.code == C.FSDP_ERR_INVALID_ARG
+    raw = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(C.FsdpError):  # f32 buffer at an odd address
+        plan.bind("fused", "f32", [raw[1:].view(torch.uint8)] * 4, check_sizes=False)
+    with pytest.raises(C.FsdpError):  # fused buffers are fp32
+        plan.bind("fused", "bf16", ok[:4], check_sizes=False)
+    b = plan.bind("shards", "bf16", ok)
+    with pytest.raises(C.FsdpError) as e:  # wrong role for the call
+        C.fsdp_rs_ar_reduce(plan, b, b)
+    assert "expected a GRADS binding" in str(e.value)
