@@ -52,6 +52,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="scale every dim 0 (small cases for profiler captures only)")
     return ap.parse_args(argv)
 
 
@@ -330,7 +332,9 @@ def run_gpu(args, wl):
     dist_init(world, "nccl")
     dev = torch.device("cuda", local)
 
-    plan = C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).upload()
+    d0 = wl.d0 if args.scale == 1.0 else scaled_workload(wl, args.scale)[0]
+    workload_name = wl.key if args.scale == 1.0 else f"{wl.key}@dim0x{args.scale:g}"
+    plan = C.Plan(d0, wl.inner, wl.rank_size, wl.shard_size).upload()
     unit = HsdpUnit(plan, wl.param_dtype, wl.grad_dtype, device=dev)
     WL.torch_fill_(unit.shards, wl.seed_params, wl.param_std, wl.param_dtype)
     WL.torch_fill_(unit.grads, wl.seed_grads, wl.grad_std, wl.grad_dtype)
@@ -391,11 +395,11 @@ def run_gpu(args, wl):
                       "bytes": kb[n], "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
     dom = max(KERNELS, key=lambda n: kernels[n]["us"])
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
-                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": ncu_traffic(dom, wl.key),
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": ncu_traffic(dom, workload_name),
                 "peak_source": peak_src}
     second = "rs_ar_reduce" if dom != "rs_ar_reduce" else "ag_copy_out"
     roofline_2 = {"bound": "hbm", "kernel": second, "achieved": kernels[second]["gbs"], "peak": peak,
-                  "unit": "GB/s", "frac": kernels[second]["frac"], "traffic": ncu_traffic(second, wl.key)}
+                  "unit": "GB/s", "frac": kernels[second]["frac"], "traffic": ncu_traffic(second, workload_name)}
 
     e2e = None
     if not args.no_e2e:
@@ -410,8 +414,8 @@ def run_gpu(args, wl):
                 "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": wl.grad_dtype, "data": "synthetic",
-                "config": {"workload": wl.key, "rank_size": wl.rank_size, "shard_size": wl.shard_size,
-                           "dp_size": plan.D, "params": wl.n_params, "elements_per_rank": sizes["N"],
+                "config": {"workload": workload_name, "rank_size": wl.rank_size,
+                           "shard_size": wl.shard_size, "dp_size": plan.D, "params": wl.n_params, "elements_per_rank": sizes["N"],
                            "step_bytes": step_bytes,
                            "l2": ("flushed between steps (2x L2 scratch write, outside the step events)"
                                   if flush else "inputs larger than L2 (working set "

@@ -27,15 +27,17 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 32, "Seg is 32 bytes on host and device");
 
-// Work is cut into warp tiles: 32 lanes x 4 steps x 8 elements. A lane
+// Work is cut into warp tiles: 32 lanes x 8 steps x 8 elements. A lane
 // moves 8 consecutive elements per step (16 B of bf16, 32 B of fp32), so a
 // warp step covers 256 consecutive elements. Granules are anchored at
 // 16-byte boundaries of the destination: a run whose first destination
 // element is not 16-byte aligned starts with a partial granule.
 constexpr int kGran = 8;
-constexpr int kSteps = 4;
-constexpr int kWarpTile = 32 * kSteps * kGran;  // 1024 elements
-constexpr int kThreads = 256;
+constexpr int kSteps = 8;
+constexpr int kStepElems = 32 * kGran;            // 256 elements
+constexpr int kWarpTile = kSteps * kStepElems;    // 2048 elements
+constexpr int kThreads = 256;                     // copy and apply kernels
+constexpr int kStagedWarps = 4;                   // warps per block, staged reduce
 
 // Work tables. Each kernel walks one: a list of runs plus, per run, the
 // index of its first warp tile (prefix sum, nseg + 1 entries).

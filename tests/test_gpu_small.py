@@ -59,6 +59,17 @@ def test_long_ragged_runs_span_many_tiles(seed):
     check_every_step(L, unit, alloc, seed=seed, ops=("avg",))
 
 
+@pytest.mark.parametrize("S,D,dts", [
+    (8, 5, ("bf16", "bf16", "bf16")),   # 40 ranks: more sources than the staged reduce holds
+    (33, 1, ("f32", "f32", "f32")),     # 33-member shard group
+    (2, 13, ("f32", "f32", "f32")),     # fp32 sources past the staged shared-memory limit
+    (16, 2, ("bf16", "bf16", "bf16")),  # 32 sources: the largest staged case
+])
+def test_wide_meshes(S, D, dts):
+    plan, L, unit, alloc = make(S, D, [70, 3, 129], [5, 16, 1], *dts)
+    check_every_step(L, unit, alloc, seed=S * 100 + D, ops=("avg",))
+
+
 @pytest.mark.parametrize("offsets", [
     # sources shifted against 16-byte boundaries, destinations aligned: funnel-shift path
     {"shards": 2, "grads": 6, "ag_output": 0},
