@@ -203,7 +203,7 @@ KArgs base_args(const fsdp_plan_s* pl, TableId t, int reps) {
     a.S = pl->S;
     a.D = pl->D;
     a.W = pl->W;
-    a.div = 1.0f;
+    set_divisor(a, 1);
     return a;
 }
 
@@ -551,7 +551,7 @@ int fsdp_apply_grads(fsdp_plan_t pl, fsdp_binding_t fused, int op, int accumulat
     a.accumulate = accumulate ? 1 : 0;
     // [OVERLAP PR #758 §二.3]: the fused buffer holds the SUM; AVG divides
     // once here, by the number of ranks that contributed (W).
-    a.div = op == FSDP_AVG ? (float)pl->W : 1.0f;
+    set_divisor(a, op == FSDP_AVG ? pl->W : 1);
     return run(K_APPLY, FSDP_F32, shard_grads->dt, a, stream, "apply_grads");
 }
 
@@ -567,7 +567,7 @@ int fsdp_rs_reduce(fsdp_plan_t pl, fsdp_binding_t rs_in, int op, fsdp_binding_t 
     a.dst_tab = fused->dev_table;
     a.vec = fused->aligned16;
     a.op = op;
-    a.div = op == FSDP_AVG ? (float)pl->S : 1.0f;
+    set_divisor(a, op == FSDP_AVG ? pl->S : 1);
     return run(K_RS, rs_in->dt, FSDP_F32, a, stream, "rs_reduce");
 }
 
@@ -584,7 +584,7 @@ int fsdp_ar_reduce(fsdp_plan_t pl, fsdp_binding_t fused, int op, fsdp_stream_t s
     a.dst_tab = fused->dev_table;
     a.vec = fused->aligned16;
     a.op = op;
-    a.div = op == FSDP_AVG ? (float)pl->D : 1.0f;
+    set_divisor(a, op == FSDP_AVG ? pl->D : 1);
     return run(K_AR, FSDP_F32, FSDP_F32, a, stream, "ar_reduce");
 }
 

@@ -82,7 +82,20 @@ struct KArgs {
     int op;                // FSDP_AVG / FSDP_SUM
     int accumulate;        // apply: add to the gradient already there
     float div;             // divisor applied after the sum (1 = none)
+    // How the divisor is applied: 0 = not at all (div == 1); 1 = multiply by
+    // recip = 1/div, an exact power of two (the exact quotient and the exact
+    // product are the same real number, so the correctly rounded results
+    // agree bit for bit, subnormals included); 2 = IEEE division.
+    int scale_mode;
+    float recip;
 };
+
+// Fills div, scale_mode and recip for a divisor d >= 1.
+inline void set_divisor(KArgs& a, int d) {
+    a.div = (float)d;
+    a.scale_mode = d == 1 ? 0 : ((d & (d - 1)) == 0 ? 1 : 2);
+    a.recip = 1.0f / (float)d;
+}
 
 enum Kind {
     K_AGIN = 0,

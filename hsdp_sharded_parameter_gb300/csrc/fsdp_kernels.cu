@@ -146,9 +146,26 @@ __device__ __forceinline__ void widen(const Raw<float>& r, float (&x)[8]) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(r.w[i]);
 }
+// Two floats to a packed bf16 pair (lo in bits 0-15) with the conversion
+// instruction's round to nearest even (subnormals kept). Its NaN result is
+// replaced by this library's NaN rule (0x7FC0 | sign).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    if (lo != lo || hi != hi) d = f32_to_bf16(lo) | (f32_to_bf16(hi) << 16);
+    return d;
+}
+
 __device__ __forceinline__ void narrow(const float (&x)[8], Raw<uint16_t>& r) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) r.w[i] = f32_to_bf16(x[2 * i]) | (f32_to_bf16(x[2 * i + 1]) << 16);
+    for (int i = 0; i < 4; ++i) r.w[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+}
+
+// The AVG divisor, applied as KArgs::scale_mode says.
+__device__ __forceinline__ float scaled(float x, const KArgs& a) {
+    if (a.scale_mode == 1) return __fmul_rn(x, a.recip);
+    if (a.scale_mode == 2) return __fdiv_rn(x, a.div);
+    return x;
 }
 __device__ __forceinline__ void narrow(const float (&x)[8], Raw<float>& r) {
 #pragma unroll
@@ -260,10 +277,35 @@ __device__ __forceinline__ D* copy_dst(const KArgs& a, const Tile& ti, int j) {
     return d + ti.dst_off;
 }
 
-template <int KIND, typename S, typename D>
+// TMA bulk copies shared -> global (bulk-group completion; the waits are
+// hardware waits, no polling).
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// Orders this thread's shared-memory writes before later async-proxy
+// (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// Dynamic shared memory of a multi-destination copy: two tile images per warp.
+template <typename D>
+constexpr size_t copy_img_bytes() {
+    return (size_t)(kThreads / 32) * 2 * kWarpTile * sizeof(D);
+}
+
+// MULTI: the kernel writes one source to several destinations (fused
+// all-gather copy-in, the gather) and has copy_img_bytes<D>() of dynamic
+// shared memory for bulk stores.
+template <int KIND, typename S, typename D, bool MULTI>
 __device__ __forceinline__ void copy_body(const KArgs& a) {
+    extern __shared__ __align__(128) uint4 copy_smem[];
     const int lane = threadIdx.x & 31;
     const int64_t stride = warp_count(), total = a.ntiles * a.reps;
+    uint4* tile_img = MULTI ? copy_smem + (size_t)(threadIdx.x >> 5) * 2 * (kWarpTile * sizeof(D) / 16) : nullptr;
+    int parity = 0;
     int64_t t = warp_id();
     int k = 0;
     Tile cur;
@@ -290,10 +332,35 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
                 }
             }
             if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
-            for (int j = 0; j < nd; ++j) {
-                D* d = copy_dst<KIND, D>(a, cur, j) + cur.rel0 + lane * kGran;
+            if (MULTI && nd > 1) {
+                // one tile image in shared memory, written to every
+                // destination by TMA bulk stores issued from lane 0; the
+                // warp's two images alternate, and an image is rewritten
+                // only after the bulk stores of two tiles ago have read it
+                uint4* img = tile_img + (size_t)parity * (kWarpTile * sizeof(D) / 16);
+                if (lane == 0) bulk_wait_read_1();
+                __syncwarp();
 #pragma unroll
-                for (int u = 0; u < kSteps; ++u) store_raw(d + u * kStepElems, val[u]);
+                for (int u = 0; u < kSteps; ++u)
+#pragma unroll
+                    for (int v = 0; v < Raw<D>::kVec; ++v)
+                        img[(u * 32 + lane) * Raw<D>::kVec + v] =
+                            make_uint4(val[u].w[4 * v], val[u].w[4 * v + 1], val[u].w[4 * v + 2], val[u].w[4 * v + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(img));
+                    for (int j = 0; j < nd; ++j)
+                        bulk_store(copy_dst<KIND, D>(a, cur, j) + cur.rel0, s, kWarpTile * (uint32_t)sizeof(D));
+                    bulk_commit();
+                }
+                parity ^= 1;
+            } else {
+                for (int j = 0; j < nd; ++j) {
+                    D* d = copy_dst<KIND, D>(a, cur, j) + cur.rel0 + lane * kGran;
+#pragma unroll
+                    for (int u = 0; u < kSteps; ++u) store_raw(d + u * kStepElems, val[u]);
+                }
             }
         } else {
             // edge tile: per-granule checks, element-wise where partial
@@ -330,6 +397,8 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
         cur = nxt;
         t = tn;
     }
+    // bulk stores still reading shared memory or writing must finish
+    if (MULTI && lane == 0) bulk_wait_all();
 }
 
 // ------------------------------------------------------------ apply kernel
@@ -338,14 +407,12 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
 // by a.div (W for AVG), optionally added to the gradient already there,
 // rounded once to the gradient dtype. rep = d.
 template <typename D>
-__device__ __forceinline__ void apply_granule(const KArgs& a, const float* src, D* dst, bool scale) {
-    Raw<float> r;
-    load_raw_at(r, reinterpret_cast<uintptr_t>(src));
+__device__ __forceinline__ void apply_granule(const KArgs& a, const Raw<float>& r, D* dst, bool scale) {
     float x[8];
     widen(r, x);
     if (scale) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = __fdiv_rn(x[e], a.div);
+        for (int e = 0; e < 8; ++e) x[e] = scaled(x[e], a);
     }
     if (a.accumulate) {
         Raw<D> old;
@@ -375,19 +442,35 @@ __device__ __forceinline__ void apply_body(const KArgs& a) {
         const float* src = static_cast<const float*>(a.src_tab[w]) + cur.src_off;
         D* dst = static_cast<D*>(a.dst_tab[(int64_t)w * a.P + cur.p]) + cur.dst_off;
         Tile nxt;
+        if (a.vec && cur.rel0 >= 0 && cur.rel0 + kWarpTile <= cur.n) {
+            // interior tile: all loads first, then the next lookup, then stores
+            Raw<float> r[kSteps];
+            const uintptr_t b = reinterpret_cast<uintptr_t>(src + cur.rel0 + lane * kGran);
+#pragma unroll
+            for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
+            if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
+#pragma unroll
+            for (int u = 0; u < kSteps; ++u)
+                apply_granule<D>(a, r[u], dst + cur.rel0 + u * kStepElems + lane * kGran, scale);
+            cur = nxt;
+            t = tn;
+            continue;
+        }
         if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
 #pragma unroll 2
         for (int u = 0; u < kSteps; ++u) {
             const int64_t rel = cur.rel0 + (int64_t)(u * kStepElems + lane * kGran);
             if (rel >= cur.n || rel + kGran <= 0) continue;
             if (a.vec && rel >= 0 && rel + kGran <= cur.n) {
-                apply_granule<D>(a, src + rel, dst + rel, scale);
+                Raw<float> r;
+                load_raw_at(r, reinterpret_cast<uintptr_t>(src + rel));
+                apply_granule<D>(a, r, dst + rel, scale);
             } else {
                 const int64_t lo = rel < 0 ? 0 : rel;
                 const int64_t hi = rel + kGran < cur.n ? rel + kGran : cur.n;
                 for (int64_t e = lo; e < hi; ++e) {
                     float q = src[e];
-                    if (scale) q = __fdiv_rn(q, a.div);
+                    if (scale) q = scaled(q, a);
                     if (a.accumulate) q = __fadd_rn(load_f32(dst, e), q);
                     store_f32(dst, e, q);
                 }
@@ -644,7 +727,7 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
         fold_fast<S>(win, lane, sh, total);
         if (scale) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) total[e] = __fdiv_rn(total[e], a.div);
+            for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
         }
         Raw<float> o;
         narrow(total, o);
@@ -687,7 +770,7 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
             }
             if (scale) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) total[e] = __fdiv_rn(total[e], a.div);
+                for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
             }
         }
         Raw<float> o;
@@ -700,7 +783,7 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
             float v = 0.0f;
             if (st.p >= 0) {
                 v = fold_elem<KIND, S>(a, sp, st.src_off + e);
-                if (scale) v = __fdiv_rn(v, a.div);
+                if (scale) v = scaled(v, a);
             }
             for (int j = 0; j < sh.nd; ++j) dp[j][e] = v;
         }
@@ -776,7 +859,7 @@ __device__ __forceinline__ void direct_reduce_body(const KArgs& a) {
                     }
                     if (scale) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) total[e] = __fdiv_rn(total[e], a.div);
+                        for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
                     }
                 }
                 Raw<float> o;
@@ -796,7 +879,7 @@ __device__ __forceinline__ void direct_reduce_body(const KArgs& a) {
                             part = s == 0 ? x : __fadd_rn(part, x);
                             if (s == s_in - 1) tot = i < s_in ? part : __fadd_rn(tot, part);
                         }
-                        v = scale ? __fdiv_rn(tot, a.div) : tot;
+                        v = scale ? scaled(tot, a) : tot;
                     }
                     for (int j = 0; j < nd; ++j) ReduceShape<KIND>::dst(a, ti.row, ti.rep, j)[ti.dst_off + e] = v;
                 }
@@ -809,13 +892,13 @@ __device__ __forceinline__ void direct_reduce_body(const KArgs& a) {
 // One named kernel per C-ABI call (the names show in profiles).
 
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D>(a); }
+__global__ void __launch_bounds__(kThreads) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D, true>(a); }
 template <typename T>
-__global__ void __launch_bounds__(kThreads) ag_gather_kernel(const KArgs a) { copy_body<K_GATHER, T, T>(a); }
+__global__ void __launch_bounds__(kThreads) ag_gather_kernel(const KArgs a) { copy_body<K_GATHER, T, T, true>(a); }
 template <typename T>
-__global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T>(a); }
+__global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
 template <typename T>
-__global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T>(a); }
+__global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
 template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(kStagedWarps * 32) rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
@@ -916,11 +999,12 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
     const bool sf = sdt == FSDP_F32, df = ddt == FSDP_F32;
     switch (kind) {
         case K_AGIN:
-            if (sf && df) return go(ag_copy_in_kernel<float, float>, a, st);
-            if (sf) return go(ag_copy_in_kernel<float, uint16_t>, a, st);
-            return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st);
+            if (sf && df) return go(ag_copy_in_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
+            if (sf) return go(ag_copy_in_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+            return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
         case K_GATHER:
-            return sf ? go(ag_gather_kernel<float>, a, st) : go(ag_gather_kernel<uint16_t>, a, st);
+            return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
+                      : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
         case K_AGOUT:
             return sf ? go(ag_copy_out_kernel<float>, a, st) : go(ag_copy_out_kernel<uint16_t>, a, st);
         case K_RSIN:
