@@ -81,6 +81,7 @@ def lib():
         L.fsdp_apply_grads.argtypes = [vp, vp, i32, i32, vp, vp]
         L.fsdp_rs_reduce.argtypes = [vp, vp, i32, vp, vp]
         L.fsdp_ar_reduce.argtypes = [vp, vp, i32, vp]
+        L.fsdp_rs_ar_reduce_noalloc.argtypes = [vp, i32, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -245,3 +246,14 @@ def fsdp_rs_reduce(plan, rs_in, op, fused, stream=None):
 
 def fsdp_ar_reduce(plan, fused, op, stream=None):
     _check(lib().fsdp_ar_reduce(plan.handle, fused.handle, OPS.get(op, op), _stream(stream)))
+
+
+def fsdp_rs_ar_reduce_noalloc(plan, grad_dt, grads, fused, stream=None):
+    """The fused gradient sync without any device allocation by the library
+    (for callers that cannot allocate device memory): ``plan`` needs no
+    upload, ``grads`` (W*P tensors) and ``fused`` (W fp32 tensors) are passed
+    as pointer arrays on every call."""
+    g = (ctypes.c_void_p * max(len(grads), 1))(*[t.data_ptr() for t in grads])
+    f = (ctypes.c_void_p * max(len(fused), 1))(*[t.data_ptr() for t in fused])
+    _check(lib().fsdp_rs_ar_reduce_noalloc(plan.handle, DTYPES.get(grad_dt, grad_dt), g, f,
+                                           _stream(stream)))

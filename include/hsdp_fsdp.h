@@ -241,6 +241,45 @@ int fsdp_rs_reduce(fsdp_plan_t plan, fsdp_binding_t rs_in, int op, fsdp_binding_
  * apply_grads (AVG) bit for bit. */
 int fsdp_ar_reduce(fsdp_plan_t plan, fsdp_binding_t fused, int op, fsdp_stream_t stream);
 
+/* ------------------------------------------------ allocation-free call */
+
+/* Size of the fixed device work area of fsdp_rs_ar_reduce_noalloc. */
+#define FSDP_NOALLOC_SCRATCH_BYTES (1 << 20)
+
+/* The fused gradient sync of fsdp_rs_ar_reduce, computing the same bits,
+ * for callers that cannot allocate device memory. The pages have no
+ * counterpart: it exists for this library's users. Who needs it: a caller
+ * whose device memory is owned wholly by its own allocator (a training
+ * framework's caching allocator, whose accounting and fragmentation control
+ * break if a library allocates on the side), or a job so close to the
+ * device's memory limit that an allocation in the middle of a step could
+ * fail. fsdp_plan_upload and fsdp_bind allocate; this call does not.
+ *
+ * plan: from fsdp_plan_create; it need not be uploaded. grad_dtype:
+ * FSDP_F32 or FSDP_BF16. grads: HOST array of W*P device pointers (index
+ * w*P + p) to the unsharded gradients, d0_p * inner_p elements each,
+ * element aligned. fused: HOST array of W device pointers to fp32 fused
+ * regions of fsdp_slice_numel(plan, FSDP_F32) elements, 4-byte aligned.
+ * Both arrays are read before the call returns.
+ *
+ * The work tables (the runs of the fused region and the two pointer tables)
+ * go to one device array of FSDP_NOALLOC_SCRATCH_BYTES that is part of the
+ * library image: every GPU that loads the library holds it until the
+ * process exits. The tables take about 40 bytes per run of the fused
+ * region (at most S * (2P + 1) runs) plus 8 bytes per buffer pointer
+ * (W * (P + 1)); a plan that needs more than FSDP_NOALLOC_SCRATCH_BYTES is
+ * refused with FSDP_ERR_INVALID_ARG and a message saying how many bytes it
+ * needs (use fsdp_rs_ar_reduce for it). The first call on a device
+ * looks up the array's device address (with that device current); make
+ * that first call before any stream capture. Every call copies its tables
+ * into the array on `stream` ahead of the kernel and rewrites everything it
+ * reads, so nothing in the array needs to start at zero; the array is
+ * shared by all calls, so calls that overlap on the GPU (different streams,
+ * no ordering between them) race on it and must not be issued. Host calls
+ * are serialised by a lock. Returns as fsdp_rs_ar_reduce does. */
+int fsdp_rs_ar_reduce_noalloc(fsdp_plan_t plan, int grad_dtype, const void* const* grads,
+                              float* const* fused, fsdp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
