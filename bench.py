@@ -401,6 +401,30 @@ def run_gpu(args, wl):
     roofline_2 = {"bound": "hbm", "kernel": second, "achieved": kernels[second]["gbs"], "peak": peak,
                   "unit": "GB/s", "frac": kernels[second]["frac"], "traffic": ncu_traffic(second, workload_name)}
 
+    # Not part of the step: the direct unshard (all three forward steps in
+    # one pass, no gathered buffer), timed alone on the same unit. It reads
+    # each shard from DRAM once (the shard-group members read the same tile
+    # within a few warps of each other, so repeats come from L2) and writes
+    # every rank's full parameters.
+    extra = {}
+    ev_u = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for _ in range(2):
+        unit.unshard_direct()
+    torch.cuda.synchronize()
+    ku = max(3, K // 4)
+    ev_u[0].record(stream)
+    for _ in range(ku):
+        if flush:
+            scratch.zero_()
+        unit.unshard_direct()
+    ev_u[1].record(stream)
+    torch.cuda.synchronize()
+    us = ev_u[0].elapsed_time(ev_u[1]) / ku * 1e3
+    ub = sizes["shard_total"] * ES[wl.param_dtype] + sizes["W"] * sizes["N"] * ES[wl.param_dtype]
+    extra["ag_unshard"] = {"us": round(us, 2), "bytes": ub, "gbs": round(ub / (us * 1e-6) / 1e9, 1),
+                           "frac": round(ub / (us * 1e-6) / 1e9 / peak, 4),
+                           "replaces_us": round(kernels["ag_copy_in"]["us"] + kernels["ag_copy_out"]["us"], 2)}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, unit, calls, step_bytes, world, dev)
@@ -421,7 +445,8 @@ def run_gpu(args, wl):
                                   if flush else "inputs larger than L2 (working set "
                                   f"{working_set / 1e9:.1f} GB >> 129 MB)"),
                            "parallelism": f"{world} independent unit(s), one per GPU"},
-                "kernels": kernels, "roofline": roofline, "roofline_second": roofline_2,
+                "kernels": kernels, "kernels_outside_step": extra,
+                "roofline": roofline, "roofline_second": roofline_2,
                 "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches}
         print(json.dumps(line), flush=True)
     unit.close()
@@ -444,13 +469,33 @@ def run_e2e(args, unit, calls, step_bytes, world, dev):
     h2d = sum(t.numel() * t.element_size() for t in ins)
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
+    # Three streams: host->device copies, the step, device->host copies.
+    # Step k+1's inputs upload while step k's results download (the link is
+    # full duplex); the step waits for its inputs and for the previous
+    # download to finish reading the outputs it overwrites; an upload waits
+    # for the previous step to finish reading the inputs it overwrites.
+    compute = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    state = {"done": None, "out": None}
+
     def one():
-        for t, h in zip(ins, h_in):
-            t.copy_(h, non_blocking=True)
+        if state["done"] is not None:
+            s_in.wait_event(state["done"])
+        with torch.cuda.stream(s_in):
+            for t, h in zip(ins, h_in):
+                t.copy_(h, non_blocking=True)
+        ev_in = s_in.record_event()
+        compute.wait_event(ev_in)
+        if state["out"] is not None:
+            compute.wait_event(state["out"])
         for c in calls:
             c()
-        for h, t in zip(h_out, outs):
-            h.copy_(t, non_blocking=True)
+        state["done"] = compute.record_event()
+        s_out.wait_event(state["done"])
+        with torch.cuda.stream(s_out):
+            for h, t in zip(h_out, outs):
+                h.copy_(t, non_blocking=True)
+        state["out"] = s_out.record_event()
 
     one()
     torch.cuda.synchronize()

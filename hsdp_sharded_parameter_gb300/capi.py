@@ -82,6 +82,7 @@ def lib():
         L.fsdp_rs_reduce.argtypes = [vp, vp, i32, vp, vp]
         L.fsdp_ar_reduce.argtypes = [vp, vp, i32, vp]
         L.fsdp_rs_ar_reduce_noalloc.argtypes = [vp, i32, vp, vp, vp]
+        L.fsdp_ag_unshard.argtypes = [vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -224,6 +225,10 @@ def fsdp_ag_gather(plan, ag_out, stream=None):
 
 def fsdp_ag_copy_out(plan, ag_out, full_params, stream=None):
     _check(lib().fsdp_ag_copy_out(plan.handle, ag_out.handle, full_params.handle, _stream(stream)))
+
+
+def fsdp_ag_unshard(plan, shards, full_params, stream=None):
+    _check(lib().fsdp_ag_unshard(plan.handle, shards.handle, full_params.handle, _stream(stream)))
 
 
 def fsdp_rs_copy_in(plan, grads, rs_in, stream=None):

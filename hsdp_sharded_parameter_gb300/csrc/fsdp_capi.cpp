@@ -98,6 +98,15 @@ void build_tables(const fsdp_plan_s& pl, std::vector<Seg> segs[T_COUNT],
                     make_seg(n, pl.off[(size_t)p * pl.S + s] * pl.inner[p], s * sl + pl.o[p], p, s));
             }
         tile_prefix(segs[T_AGOUT_F32 + i], es, tiles[T_AGOUT_F32 + i]);
+        // direct unshard: shard s of parameter p (held by shard-group member
+        // s) goes to rows [off, off+len) of p, no gathered buffer in between
+        for (int p = 0; p < pl.P; ++p)
+            for (int s = 0; s < pl.S; ++s) {
+                int64_t n = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
+                if (n == 0) continue;
+                segs[T_UNSHARD_F32 + i].push_back(make_seg(n, pl.off[(size_t)p * pl.S + s] * pl.inner[p], 0, p, s));
+            }
+        tile_prefix(segs[T_UNSHARD_F32 + i], es, tiles[T_UNSHARD_F32 + i]);
         // RS copy-in: row s of the RS input, from the full gradients
         for (int s = 0; s < pl.S; ++s) row_runs(pl, s, s * sl, sl, true, segs[T_RSIN_F32 + i]);
         tile_prefix(segs[T_RSIN_F32 + i], es, tiles[T_RSIN_F32 + i]);
@@ -505,6 +514,21 @@ int fsdp_ag_copy_out(fsdp_plan_t pl, fsdp_binding_t ag_out, fsdp_binding_t full,
     a.dst_tab = full->dev_table;
     a.vec = full->aligned16;
     return run(K_AGOUT, ag_out->dt, full->dt, a, stream, "ag_copy_out");
+}
+
+int fsdp_ag_unshard(fsdp_plan_t pl, fsdp_binding_t shards, fsdp_binding_t full, fsdp_stream_t stream) {
+    clear_error();
+    int rc;
+    if ((rc = check_ready(pl, "ag_unshard"))) return rc;
+    if ((rc = check_binding(pl, shards, FSDP_ROLE_SHARDS, "ag_unshard"))) return rc;
+    if ((rc = check_binding(pl, full, FSDP_ROLE_FULL_PARAMS, "ag_unshard"))) return rc;
+    if (shards->dt == FSDP_BF16 && full->dt == FSDP_F32)
+        return set_error(FSDP_ERR_INVALID_ARG, "ag_unshard: bf16 shards cannot be gathered as f32");
+    KArgs a = base_args(pl, full->dt == FSDP_F32 ? T_UNSHARD_F32 : T_UNSHARD_BF16, pl->W);
+    a.src_tab = shards->dev_table;
+    a.dst_tab = full->dev_table;
+    a.vec = full->aligned16;
+    return run(K_UNSHARD, shards->dt, full->dt, a, stream, "ag_unshard");
 }
 
 int fsdp_rs_copy_in(fsdp_plan_t pl, fsdp_binding_t grads, fsdp_binding_t rs_in, fsdp_stream_t stream) {

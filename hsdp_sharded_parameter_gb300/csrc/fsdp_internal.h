@@ -55,6 +55,8 @@ enum TableId {
     T_RS_F32,          // unfused RS: row s of an f32 RS input
     T_RS_BF16,         //             row s of a bf16 RS input
     T_AR,              // unfused AR: fp32 fused region, per s
+    T_UNSHARD_F32,     // direct unshard: (p, s) shards into the full parameters
+    T_UNSHARD_BF16,
     T_COUNT
 };
 
@@ -105,7 +107,8 @@ enum Kind {
     K_RSAR,
     K_RS,
     K_AR,
-    K_APPLY
+    K_APPLY,
+    K_UNSHARD
 };
 
 // Launches the kernel of `kind` for the given element types. Returns a

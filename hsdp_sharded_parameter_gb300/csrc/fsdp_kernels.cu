@@ -253,6 +253,8 @@ __device__ __forceinline__ const S* copy_src(const KArgs& a, const Tile& ti) {
                          : nullptr;
     if (KIND == K_GATHER) return static_cast<const S*>(a.src_tab[ti.rep * a.S + ti.row]);
     if (KIND == K_AGOUT) return static_cast<const S*>(a.src_tab[ti.rep]);
+    if (KIND == K_UNSHARD)
+        return static_cast<const S*>(a.src_tab[(int64_t)((ti.rep / a.S) * a.S + ti.row) * a.P + ti.p]);
     return ti.p >= 0 ? static_cast<const S*>(a.src_tab[(int64_t)ti.rep * a.P + ti.p]) : nullptr;
 }
 
@@ -270,7 +272,7 @@ __device__ __forceinline__ D* copy_dst(const KArgs& a, const Tile& ti, int j) {
         d = static_cast<D*>(a.dst_tab[ti.rep * a.S + (a.fuse ? j : ti.row)]);
     else if (KIND == K_GATHER)
         d = static_cast<D*>(a.dst_tab[ti.rep * a.S + j + (j >= ti.row ? 1 : 0)]);
-    else if (KIND == K_AGOUT)
+    else if (KIND == K_AGOUT || KIND == K_UNSHARD)
         d = static_cast<D*>(a.dst_tab[(int64_t)ti.rep * a.P + ti.p]);
     else
         d = static_cast<D*>(a.dst_tab[ti.rep]);
@@ -899,6 +901,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
+template <typename S, typename D>
+__global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, false>(a); }
 template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(kStagedWarps * 32) rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
@@ -1005,6 +1009,10 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
         case K_GATHER:
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
                       : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+        case K_UNSHARD:
+            if (sf && df) return go(ag_unshard_kernel<float, float>, a, st);
+            if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st);
+            return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st);
         case K_AGOUT:
             return sf ? go(ag_copy_out_kernel<float>, a, st) : go(ag_copy_out_kernel<uint16_t>, a, st);
         case K_RSIN:

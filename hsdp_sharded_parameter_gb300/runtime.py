@@ -68,6 +68,10 @@ class HsdpUnit:
     def ag_copy_out(self, stream=None):
         C.fsdp_ag_copy_out(self.plan, self.b_ag, self.b_full, stream)
 
+    def unshard_direct(self, stream=None):
+        """All three forward steps in one kernel, no gathered buffer."""
+        C.fsdp_ag_unshard(self.plan, self.b_shards, self.b_full, stream)
+
     def unshard(self, fuse_gather=True, stream=None):
         self.ag_copy_in(fuse_gather, stream)
         if not fuse_gather:

@@ -196,6 +196,16 @@ int fsdp_ag_gather(fsdp_plan_t plan, fsdp_binding_t ag_out, fsdp_stream_t stream
 int fsdp_ag_copy_out(fsdp_plan_t plan, fsdp_binding_t ag_out, fsdp_binding_t full_params,
                      fsdp_stream_t stream);
 
+/* Direct unshard, all three forward steps in one pass without the gathered
+ * buffer (the follow-up "option 2" of [OVERLAP PR #758 §四, on ag_output]:
+ * unsharded parameters filled straight from the shards): rank (d, s)'s
+ * full parameter p gets, at rows [off_{p,s'}, off_{p,s'} + len_{p,s'}),
+ * shard s' of p held by shard-group member (d, s'), cast as in
+ * fsdp_ag_copy_in. The result equals fsdp_ag_copy_in + fsdp_ag_gather +
+ * fsdp_ag_copy_out bit for bit; no AG_OUTPUT buffer is needed. */
+int fsdp_ag_unshard(fsdp_plan_t plan, fsdp_binding_t shards, fsdp_binding_t full_params,
+                    fsdp_stream_t stream);
+
 /* ------------------------------------------------- backward (grad sync) */
 
 /* Reduce-scatter copy-in [RAGGED §6.4; OVERLAP PR #758 §二.1]: row s' of

@@ -142,6 +142,13 @@ def check_every_step(L, unit, alloc, seed=0, special=False, ops=("avg", "sum")):
     for g, r in zip(unit.full, ref_full):
         assert cmp(to_np(g), r, adt), "ag_copy_out"
         n += 1
+    # forward in one pass, straight from the shards
+    dirty(unit.full)
+    unit.unshard_direct()
+    torch.cuda.synchronize()
+    for g, r in zip(unit.full, ref_full):
+        assert cmp(to_np(g), r, adt), "ag_unshard"
+        n += 1
     # forward, fused copy-in + gather on a dirty buffer
     dirty(unit.ag_out)
     unit.ag_copy_in(fuse_gather=True)

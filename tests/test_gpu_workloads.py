@@ -173,6 +173,21 @@ def test_workload_full_size(key):
     free(unit, plan)
 
 
+@pytest.mark.parametrize("key", ["ragged_fsdp", "large_hsdp"])
+def test_direct_unshard_full_size(key):
+    # all three forward steps in one pass must give the same full parameters
+    wl, plan, L, unit = build(key)
+    unit.unshard_direct()
+    torch.cuda.synchronize()
+    S, P = L.S, L.P
+    for w in range(L.W):
+        d = w // S
+        for p in range(P):
+            parts = [unit.shards[(d * S + sp) * P + p] for sp in range(S)]
+            assert torch.equal(bits(unit.full[w * P + p]), bits(torch.cat(parts))), (w, p)
+    free(unit, plan)
+
+
 def test_pure_tp_sum_op():
     # the DTensor-managed (pure TP) default is SUM ("Hyper通信掩盖方案" PR #758 §二.3)
     wl, plan, L, unit = build("pure_tp_compat")
