@@ -43,6 +43,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxStagedSources = 32;
+// Resident blocks of the staged reduce its shared memory allows for 16 bf16
+// sources (69 KB each); telling the compiler so lets it keep the unrolled
+// fold in registers (up to 170 each) instead of spilling.
+constexpr int kStagedBlocksPerSm = 3;
 
 // ------------------------------------------------------------------ scalars
 
@@ -109,6 +113,41 @@ __device__ __forceinline__ void load_raw_at(Raw<T>& r, uintptr_t a) {
         for (int v = 0; v <= Raw<T>::kVec; ++v) blk[v] = ld_reuse(q + v);
 #pragma unroll
         for (int v = 0; v < Raw<T>::kVec; ++v) put(r.w + 4 * v, funnel(blk[v], blk[v + 1], sh));
+    }
+}
+
+// One warp step (256 elements) whose source is shifted by sh (1..15) bytes
+// against the destination granules. w0 is the aligned start of the step's
+// source window (33 or 65 blocks). Lane l loads its own aligned blocks and
+// takes the next one from lane l+1 (lane 31 loads it), so every source
+// block is loaded once; all 32 lanes must take part.
+// All kSteps steps of an interior tile are loaded first and shuffled after:
+// a warp-synchronous shuffle keeps later loads from being issued ahead of
+// it, so interleaving them would expose one memory latency per step. step
+// is the byte distance between consecutive steps' windows.
+template <typename T>
+__device__ __forceinline__ void load_tile_shifted(Raw<T> (&r)[kSteps], uintptr_t w0, uintptr_t step,
+                                                  unsigned sh, int lane) {
+    constexpr int kV = Raw<T>::kVec;
+    uint4 blk[kSteps][kV];
+    uint4 last[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+        const uint4* q = reinterpret_cast<const uint4*>(w0 + u * step) + lane * kV;
+#pragma unroll
+        for (int v = 0; v < kV; ++v) blk[u][v] = ld_stream(q + v);
+        last[u] = lane == 31 ? ld_stream(q + kV) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+        uint4 nx;
+        nx.x = __shfl_down_sync(kFull, blk[u][0].x, 1);
+        nx.y = __shfl_down_sync(kFull, blk[u][0].y, 1);
+        nx.z = __shfl_down_sync(kFull, blk[u][0].z, 1);
+        nx.w = __shfl_down_sync(kFull, blk[u][0].w, 1);
+        if (lane == 31) nx = last[u];
+#pragma unroll
+        for (int v = 0; v < kV; ++v) put(r[u].w + 4 * v, funnel(blk[u][v], v + 1 < kV ? blk[u][v + 1] : nx, sh));
     }
 }
 
@@ -324,13 +363,21 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
 #pragma unroll
                 for (int u = 0; u < kSteps; ++u) zero_raw(val[u]);
             } else {
-                const uintptr_t b = reinterpret_cast<uintptr_t>(src + cur.src_off + cur.rel0) +
-                                    (uintptr_t)(lane * kGran * (int)sizeof(S));
+                const uintptr_t t0 = reinterpret_cast<uintptr_t>(src + cur.src_off + cur.rel0);
+                const unsigned sh = (unsigned)(t0 & 15u);
+                if (sh == 0) {
+                    const uintptr_t b = t0 + (uintptr_t)(lane * kGran * (int)sizeof(S));
 #pragma unroll
-                for (int u = 0; u < kSteps; ++u) {
-                    Raw<S> r;
-                    load_raw_at(r, b + (uintptr_t)(u * kStepElems * (int)sizeof(S)));
-                    convert(r, val[u]);
+                    for (int u = 0; u < kSteps; ++u) {
+                        Raw<S> r;
+                        load_raw_at(r, b + (uintptr_t)(u * kStepElems * (int)sizeof(S)));
+                        convert(r, val[u]);
+                    }
+                } else {
+                    Raw<S> r[kSteps];
+                    load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * (int)sizeof(S)), sh, lane);
+#pragma unroll
+                    for (int u = 0; u < kSteps; ++u) convert(r[u], val[u]);
                 }
             }
             if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
@@ -447,9 +494,15 @@ __device__ __forceinline__ void apply_body(const KArgs& a) {
         if (a.vec && cur.rel0 >= 0 && cur.rel0 + kWarpTile <= cur.n) {
             // interior tile: all loads first, then the next lookup, then stores
             Raw<float> r[kSteps];
-            const uintptr_t b = reinterpret_cast<uintptr_t>(src + cur.rel0 + lane * kGran);
+            const uintptr_t t0 = reinterpret_cast<uintptr_t>(src + cur.rel0);
+            const unsigned sh = (unsigned)(t0 & 15u);
+            if (sh == 0) {
+                const uintptr_t b = t0 + (uintptr_t)(lane * kGran * 4);
 #pragma unroll
-            for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
+                for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
+            } else {
+                load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * 4), sh, lane);
+            }
             if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
 #pragma unroll
             for (int u = 0; u < kSteps; ++u)
@@ -545,7 +598,8 @@ struct Step {
     int64_t n, dst_off, src_off, rel;  // rel: run-relative element of lane 0's granule
     int p, row, rep;
     bool valid;
-    bool fast;  // interior data step whose every source is 16-byte aligned at its start
+    bool fast;       // interior data step whose sources all share one 16-byte shift
+    unsigned shift;  // that shift in bytes (0 = aligned)
 };
 
 // Yields a warp's steps in order: its tiles (grid stride), 8 steps each,
@@ -566,6 +620,7 @@ struct StepGen {
         Step s;
         s.valid = false;
         s.fast = false;
+        s.shift = 0;
         for (;;) {
             if (t >= total) return s;
             if (++u == kSteps) {
@@ -632,18 +687,24 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
     if (st.valid && st.p >= 0 && a.vec) {
         const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(win));
         const int64_t byte0 = (st.src_off + st.rel) * (int64_t)sizeof(S);  // may precede the run: address only
+        const unsigned sh0 = (unsigned)((reinterpret_cast<uintptr_t>(sp[0]) + (uintptr_t)byte0) & 15u);
         bool ok = true;
         for (int i = lane; i < sh.ns; i += 32)
-            ok = ok && ((reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)byte0) & 15u) == 0;
-        const bool aligned = __all_sync(kFull, ok);
-        if (aligned && st.rel >= 0 && st.rel + kStepElems <= st.n) {
+            ok = ok && ((reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)byte0) & 15u) == sh0;
+        const bool uniform = __all_sync(kFull, ok);
+        if (uniform && st.rel >= 0 && st.rel + kStepElems <= st.n) {
+            // every source window starts sh0 bytes before its first element;
+            // a shifted window needs one block more, copied by lane 0
             st.fast = true;
+            st.shift = sh0;
 #pragma unroll
             for (int i = 0; i < sh.ns; ++i) {
-                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0;
+                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0 - sh0;
 #pragma unroll
                 for (int v = 0; v < Raw<S>::kVec; ++v)
                     cp_async16(sbase + (uint32_t)((i * kWin + lane + 32 * v) * 16), g + (lane + 32 * v) * 16);
+                if (sh0 != 0 && lane == 0)
+                    cp_async16(sbase + (uint32_t)((i * kWin + kWin - 1) * 16), g + (kWin - 1) * 16);
             }
         } else {
             const int64_t e_lo = st.rel < 0 ? 0 : st.rel;
@@ -680,11 +741,11 @@ __device__ __forceinline__ void read_window(const uint4* win, int i, int lane, u
     }
 }
 
-// Interior step of aligned sources: every lane's granule is full; source i
-// of lane l sits at window blocks [l*kVec, (l+1)*kVec).
-template <typename S, int NS, int SIN, int ND, int KIND>
-__device__ __forceinline__ void fold_fast(const uint4* win, int lane, const Shape<KIND, NS, SIN, ND>& sh,
-                                          float (&total)[8]) {
+// Interior step whose sources share one shift: every lane's granule is
+// full; source i of lane l starts `shift` bytes into window block l*kVec.
+template <bool SHIFTED, typename S, int NS, int SIN, int ND, int KIND>
+__device__ __forceinline__ void fold_fast(const uint4* win, int lane, unsigned shift,
+                                          const Shape<KIND, NS, SIN, ND>& sh, float (&total)[8]) {
 #pragma unroll
     for (int d = 0; d < sh.d_out; ++d) {
         float part[8];
@@ -692,8 +753,16 @@ __device__ __forceinline__ void fold_fast(const uint4* win, int lane, const Shap
         for (int s = 0; s < sh.s_in; ++s) {
             const uint4* w = win + (d * sh.s_in + s) * Staging<S>::kWin + lane * Raw<S>::kVec;
             Raw<S> r;
+            if (SHIFTED) {
+                uint4 blk[Raw<S>::kVec + 1];
 #pragma unroll
-            for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, w[v]);
+                for (int v = 0; v <= Raw<S>::kVec; ++v) blk[v] = w[v];
+#pragma unroll
+                for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, funnel(blk[v], blk[v + 1], shift));
+            } else {
+#pragma unroll
+                for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, w[v]);
+            }
             float x[8];
             widen(r, x);
             if (s == 0) {
@@ -726,7 +795,10 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
     const bool scale = a.div != 1.0f;
     if (st.fast) {
         float total[8];
-        fold_fast<S>(win, lane, sh, total);
+        if (st.shift == 0)
+            fold_fast<false, S>(win, lane, 0u, sh, total);
+        else
+            fold_fast<true, S>(win, lane, st.shift, sh, total);
         if (scale) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
@@ -904,15 +976,15 @@ __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { c
 template <typename S, typename D>
 __global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, false>(a); }
 template <typename S, int NS, int SIN, int ND>
-__global__ void __launch_bounds__(kStagedWarps * 32) rs_ar_reduce_kernel(const KArgs a) {
+__global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
 }
 template <typename S, int NS>
-__global__ void __launch_bounds__(kStagedWarps * 32) rs_reduce_kernel(const KArgs a) {
+__global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RS, S, NS, NS, 1>(a);
 }
 template <int NS>
-__global__ void __launch_bounds__(kStagedWarps * 32) ar_reduce_kernel(const KArgs a) {
+__global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_AR, float, NS, 1, NS>(a);
 }
 template <typename S>
