@@ -62,6 +62,7 @@ def lib():
         L.fsdp_last_error.restype = ctypes.c_char_p
         L.fsdp_launch_count.restype = ctypes.c_uint64
         L.fsdp_plan_create.argtypes = [i32, vp, vp, i32, i32, i32, i32, P(vp)]
+        L.fsdp_plan_create_bucketed.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, P(vp)]
         L.fsdp_plan_destroy.argtypes = [vp]
         L.fsdp_plan_upload.argtypes = [vp]
         L.fsdp_plan_info.argtypes = [vp, P(i32), P(i32), P(i32), P(i32), P(i64)]
@@ -109,15 +110,18 @@ def fsdp_launch_count():
 class Plan:
     """Owns an fsdp_plan_t. Host-only until ``upload()``."""
 
-    def __init__(self, dim0, inner, rank_size, shard_size, enable_param_shard=1, shard_dim=0):
+    def __init__(self, dim0, inner, rank_size, shard_size, enable_param_shard=1, shard_dim=0,
+                 bucket=None):
         import numpy as np
 
         self._d0 = np.ascontiguousarray(dim0, dtype=np.int64)
         self._inner = np.ascontiguousarray(inner, dtype=np.int64)
+        self._bucket = None if bucket is None else np.ascontiguousarray(bucket, dtype=np.int32)
         h = ctypes.c_void_p()
-        _check(lib().fsdp_plan_create(len(self._d0), self._d0.ctypes.data, self._inner.ctypes.data,
-                                      rank_size, shard_size, enable_param_shard, shard_dim,
-                                      ctypes.byref(h)))
+        _check(lib().fsdp_plan_create_bucketed(
+            len(self._d0), self._d0.ctypes.data, self._inner.ctypes.data,
+            None if self._bucket is None else self._bucket.ctypes.data,
+            rank_size, shard_size, enable_param_shard, shard_dim, ctypes.byref(h)))
         self.handle = h
         W, S, D, P = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
         sp = ctypes.c_int64()

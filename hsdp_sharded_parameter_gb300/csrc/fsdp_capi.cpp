@@ -234,6 +234,13 @@ uint64_t fsdp_launch_count(void) { return g_launches.load(std::memory_order_rela
 
 int fsdp_plan_create(int n_params, const int64_t* dim0, const int64_t* inner, int rank_size,
                      int shard_size, int enable_param_shard, int shard_dim, fsdp_plan_t* out) {
+    return fsdp_plan_create_bucketed(n_params, dim0, inner, nullptr, rank_size, shard_size,
+                                     enable_param_shard, shard_dim, out);
+}
+
+int fsdp_plan_create_bucketed(int n_params, const int64_t* dim0, const int64_t* inner, const int* bucket,
+                              int rank_size, int shard_size, int enable_param_shard, int shard_dim,
+                              fsdp_plan_t* out) {
     clear_error();
     if (!out) return set_error(FSDP_ERR_INVALID_ARG, "plan_create: out is NULL");
     *out = nullptr;
@@ -260,12 +267,22 @@ int fsdp_plan_create(int n_params, const int64_t* dim0, const int64_t* inner, in
     pl->off.resize((size_t)n_params * S);
     pl->len.resize((size_t)n_params * S);
     pl->o.assign(n_params + 1, 0);
+    int64_t end = 0;  // end of the previous parameter's padded region
     for (int p = 0; p < n_params; ++p) {
         if (dim0[p] < 0 || inner[p] < 1) {
             delete pl;
             return set_error(FSDP_ERR_INVALID_ARG, "plan_create: parameter " + std::to_string(p) +
                                                        " needs dim0 >= 0 and inner >= 1");
         }
+        if (bucket && (bucket[p] < 0 || (p > 0 && bucket[p] < bucket[p - 1]))) {
+            delete pl;
+            return set_error(FSDP_ERR_INVALID_ARG,
+                             "plan_create: bucket ids must be >= 0 and follow the registration order");
+        }
+        // [OVERLAP PR #758 §二.1, AllReduceParamGroup]: a new bucket starts
+        // at the next multiple of 256 elements (512 B in bf16 and in fp32).
+        if (bucket && p > 0 && bucket[p] != bucket[p - 1]) end = (end + 255) / 256 * 256;
+        pl->o[p] = end;
         // [RAGGED §6.4]: chunk = ceil(dim0 / S); shard s starts at
         // min(s * chunk, dim0) and holds min(chunk, dim0 - start) rows.
         const int64_t c = (dim0[p] + S - 1) / S;
@@ -276,9 +293,10 @@ int fsdp_plan_create(int n_params, const int64_t* dim0, const int64_t* inner, in
             pl->len[(size_t)p * S + s] = std::min<int64_t>(c, dim0[p] - start);
         }
         // The slice offset advances by padded_sharded_param_size.numel().
-        pl->o[p + 1] = pl->o[p] + c * inner[p];
+        end = pl->o[p] + c * inner[p];
     }
-    pl->sum_padded = pl->o[n_params];
+    pl->o[n_params] = end;
+    pl->sum_padded = end;
     *out = pl;
     return FSDP_OK;
 }

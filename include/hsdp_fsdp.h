@@ -22,7 +22,8 @@
  *   shard s of p holds rows [off_{p,s}, off_{p,s} + len_{p,s}) with
  *   off = min(s*chunk, d0), len = min(chunk, d0 - off) ("sharded_size",
  *   possibly 0) [RAGGED §6.4]. Inside a per-rank slice parameter p starts at
- *   o_p = sum_{q<p} chunk_q * inner_q and occupies chunk_p * inner_p
+ *   o_p = sum_{q<p} chunk_q * inner_q (one bucket; several buckets: see
+ *   fsdp_plan_create_bucketed) and occupies chunk_p * inner_p
  *   elements; the rows past len are zero. A slice holds slice(dt) elements:
  *   sum_p chunk_p*inner_p rounded up to a multiple of 512 bytes [OVERLAP
  *   PR #758 §二.1, the 512B-aligned fused buffer].
@@ -116,6 +117,18 @@ uint64_t fsdp_launch_count(void);
  * Needs no GPU. *out receives a handle owned by the caller. */
 int fsdp_plan_create(int n_params, const int64_t* dim0, const int64_t* inner, int rank_size,
                      int shard_size, int enable_param_shard, int shard_dim, fsdp_plan_t* out);
+
+/* As fsdp_plan_create, for several buckets sharing one fused buffer: the
+ * AllReduceParamGroup of [OVERLAP PR #758 §二.1], which gathers the buckets
+ * of one replicate group into a single 512-byte-aligned fused all-reduce.
+ * bucket[p] >= 0 is parameter p's bucket, non-decreasing in registration
+ * order (NULL = one bucket). Every per-rank slice holds the buckets in
+ * order; a bucket starts at the next multiple of 256 elements (512 bytes
+ * in bf16, 1024 in fp32), its parameters packed as in a one-bucket plan,
+ * the gaps zero. One call of each data function then covers all buckets. */
+int fsdp_plan_create_bucketed(int n_params, const int64_t* dim0, const int64_t* inner,
+                              const int* bucket, int rank_size, int shard_size,
+                              int enable_param_shard, int shard_dim, fsdp_plan_t* out);
 
 /* Frees the plan and its device tables. The caller must ensure no enqueued
  * work still uses them (e.g. synchronise the streams first). NULL is a no-op. */

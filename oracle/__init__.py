@@ -50,6 +50,7 @@ def lib():
         L = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.hor_plan.argtypes = [i32, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        L.hor_plan_bucketed.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         L.hor_effective_shard_size.argtypes = [i32, i32]
         L.hor_slice_numel.argtypes = [i64, i32]
         L.hor_slice_numel.restype = i64
@@ -104,8 +105,10 @@ def _check(code, what):
 class Layout:
     """The oracle's plan: chunk rows, shard ranges and slice offsets."""
 
-    def __init__(self, d0, inner, rank_size, shard_size, enable_param_shard=1, shard_dim=0):
+    def __init__(self, d0, inner, rank_size, shard_size, enable_param_shard=1, shard_dim=0,
+                 bucket=None):
         L = lib()
+        self.bucket = None if bucket is None else np.ascontiguousarray(bucket, dtype=np.int32)
         self.d0 = np.ascontiguousarray(d0, dtype=np.int64)
         self.inner = np.ascontiguousarray(inner, dtype=np.int64)
         self.P = len(self.d0)
@@ -116,9 +119,10 @@ class Layout:
         self.off = np.zeros((max(self.P, 1), S), np.int64)
         self.len = np.zeros((max(self.P, 1), S), np.int64)
         self.o = np.zeros(self.P + 1, np.int64)
-        code = L.hor_plan(self.P, _ptr(self.d0), _ptr(self.inner), self.W, shard_size,
-                          enable_param_shard, shard_dim, _ptr(self.dss), _ptr(self.off),
-                          _ptr(self.len), _ptr(self.o))
+        code = L.hor_plan_bucketed(self.P, _ptr(self.d0), _ptr(self.inner),
+                                   None if self.bucket is None else _ptr(self.bucket), self.W,
+                                   shard_size, enable_param_shard, shard_dim, _ptr(self.dss),
+                                   _ptr(self.off), _ptr(self.len), _ptr(self.o))
         _check(code, "plan")
         self.dss = self.dss[: self.P]
         self.off = self.off[: self.P]

@@ -127,6 +127,14 @@ int hor_plan(int P, const int64_t* d0, const int64_t* inner, int rank_size,
              int shard_size, int enable_param_shard, int shard_dim,
              int64_t* dss, int64_t* off, int64_t* len, int64_t* o)
 {
+    return hor_plan_bucketed(P, d0, inner, NULL, rank_size, shard_size, enable_param_shard,
+                             shard_dim, dss, off, len, o);
+}
+
+int hor_plan_bucketed(int P, const int64_t* d0, const int64_t* inner, const int* bucket,
+                      int rank_size, int shard_size, int enable_param_shard, int shard_dim,
+                      int64_t* dss, int64_t* off, int64_t* len, int64_t* o)
+{
     if (P < 0 || rank_size < 1 || (P > 0 && (!d0 || !inner)))
         return HOR_EINVAL;
     int S = hor_effective_shard_size(shard_size, enable_param_shard);
@@ -138,10 +146,19 @@ int hor_plan(int P, const int64_t* d0, const int64_t* inner, int rank_size,
      * this layout describes dim 0 only. */
     if (shard_dim != 0)
         return HOR_ENOTIMPL;
-    o[0] = 0;
+    int64_t end = 0; /* end of the previous parameter's padded region */
     for (int p = 0; p < P; ++p) {
         if (d0[p] < 0 || inner[p] < 1)
             return HOR_EINVAL;
+        /* [OVERLAP] PR #758 write-up §二.1 (AllReduceParamGroup): several
+         * buckets share one fused buffer. Reading: bucket ids rise with the
+         * registration order and a new bucket starts at the next multiple of
+         * 256 elements, a 512-byte boundary in bf16 and in fp32 alike. */
+        if (bucket && (bucket[p] < 0 || (p > 0 && bucket[p] < bucket[p - 1])))
+            return HOR_EINVAL;
+        if (bucket && p > 0 && bucket[p] != bucket[p - 1])
+            end = (end + 255) / 256 * 256;
+        o[p] = end;
         /* [RAGGED] §6.4: fixed-size chunks of ceil(dim0 / S) rows; shard s
          * starts at min(s * chunk, dim0) and holds min(chunk, dim0 - start)
          * rows, which may be 0. */
@@ -159,8 +176,9 @@ int hor_plan(int P, const int64_t* d0, const int64_t* inner, int rank_size,
         }
         /* [RAGGED] §6.4 "AllGather 和 ReduceScatter": the offset inside the
          * fused buffer advances by padded_sharded_param_size.numel(). */
-        o[p + 1] = o[p] + chunk * inner[p];
+        end = o[p] + chunk * inner[p];
     }
+    o[P] = end;
     return HOR_OK;
 }
 
@@ -418,7 +436,7 @@ int hor_locate_fused(const hor_layout* L, int s, int64_t j, int64_t* e)
      * parameter whose padded region holds j, then the row inside shard s.
      * Returns the parameter index, or -1 when j is padding. */
     for (int p = 0; p < L->P; ++p) {
-        if (j >= L->o[p] && j < L->o[p + 1]) {
+        if (j >= L->o[p] && j < L->o[p] + L->dss[p] * L->inner[p]) {
             int64_t rel = j - L->o[p];
             int64_t i = rel / L->inner[p], c = rel % L->inner[p];
             if (i >= L->len[(int64_t)p * L->S + s])
@@ -437,7 +455,7 @@ int hor_locate_slice(const hor_layout* L, int s, int64_t j, int64_t* k)
      * j - o_p of its shard when that lies inside the actual rows. Returns
      * the parameter index, or -1 when j is padding. */
     for (int p = 0; p < L->P; ++p) {
-        if (j >= L->o[p] && j < L->o[p + 1]) {
+        if (j >= L->o[p] && j < L->o[p] + L->dss[p] * L->inner[p]) {
             int64_t rel = j - L->o[p];
             if (rel >= L->len[(int64_t)p * L->S + s] * L->inner[p])
                 return -1;

@@ -20,7 +20,7 @@ typedef struct {
     const int64_t* dss;   /* [P] padded shard rows = ceil(d0 / S) */
     const int64_t* off;   /* [P*S] first row of shard s of param p (p*S + s) */
     const int64_t* len;   /* [P*S] rows held by shard s of param p */
-    const int64_t* o;     /* [P+1] element offset of param p inside a slice */
+    const int64_t* o;     /* [P+1] element offset of param p inside a slice; o[P] = end */
 } hor_layout;
 
 float hor_bf16_to_f32(uint16_t h);
@@ -30,6 +30,9 @@ int hor_effective_shard_size(int shard_size, int enable_param_shard);
 int hor_plan(int P, const int64_t* d0, const int64_t* inner, int rank_size,
              int shard_size, int enable_param_shard, int shard_dim,
              int64_t* dss, int64_t* off, int64_t* len, int64_t* o);
+int hor_plan_bucketed(int P, const int64_t* d0, const int64_t* inner, const int* bucket,
+                      int rank_size, int shard_size, int enable_param_shard, int shard_dim,
+                      int64_t* dss, int64_t* off, int64_t* len, int64_t* o);
 int64_t hor_slice_numel(int64_t sum_padded, int dt);
 void hor_group_ranks(int W, int S, int w, int* shard_group, int* replicate_group);
 void hor_comm_calls(int S, int D, int* rs_group_size, int* ar_group_size);

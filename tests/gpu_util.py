@@ -98,6 +98,8 @@ def same_values(a, b, dt):
 
 
 def make(S, D, d0, inner, param_dt="bf16", grad_dt="bf16", ag_dt=None, offsets=None, **plan_kw):
+    """A unit over guarded buffers and the oracle's layout of the same plan
+    (plan_kw: enable_param_shard, bucket)."""
     plan = C.Plan(d0, inner, S * D, S, **plan_kw).upload()
     L = O.Layout(d0, inner, S * D, S, **plan_kw)
     alloc = GuardedAlloc(offsets)

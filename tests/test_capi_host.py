@@ -90,3 +90,20 @@ def test_upload_without_gpu_fails_cleanly():
     with pytest.raises(C.FsdpError) as e:
         cp.upload()
     assert e.value.code in (C.FSDP_ERR_CUDA, C.FSDP_ERR_NOMEM)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bucketed_plans_equal_oracle(seed):
+    rng = np.random.default_rng(seed)
+    P = int(rng.integers(1, 25))
+    S, D = int(rng.integers(1, 9)), int(rng.integers(1, 4))
+    d0 = [int(x) for x in rng.integers(0, 500, P)]
+    inner = [int(x) for x in rng.choice([1, 2, 5, 64, 128], P)]
+    bucket = sorted(int(x) for x in rng.integers(0, 5, P))
+    same_plan(C.Plan(d0, inner, S * D, S, bucket=bucket), O.Layout(d0, inner, S * D, S, bucket=bucket))
+
+
+def test_bucket_order_is_checked():
+    with pytest.raises(C.FsdpError) as e:
+        C.Plan([4, 4], [1, 1], 4, 4, bucket=[1, 0])
+    assert e.value.code == C.FSDP_ERR_INVALID_ARG and "bucket" in str(e.value)

@@ -148,3 +148,14 @@ def test_bad_bindings_are_refused():
     with pytest.raises(C.FsdpError) as e:  # wrong role for the call
         C.fsdp_rs_ar_reduce(plan, b, b)
     assert "expected a GRADS binding" in str(e.value)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_bucketed_plans(seed):
+    # several buckets in one fused buffer ("Hyper通信掩盖方案" PR #758 §二.1,
+    # AllReduceParamGroup): every call covers all buckets, gaps stay zero
+    S, D, d0, inner, pdt, gdt, adt = random_plan(1000 + seed)
+    rng = np.random.default_rng(seed)
+    bucket = sorted(int(x) for x in rng.integers(0, 4, len(d0)))
+    plan, L, unit, alloc = make(S, D, d0, inner, pdt, gdt, adt, bucket=bucket)
+    check_every_step(L, unit, alloc, seed=seed)

@@ -515,3 +515,68 @@ def test_locators_agree_with_whole_buffer_steps(S, D, d0, inner):
             d = w // S
             src = np.array([shards[(d * S + sh[i]) * L.P + q][k[i]] for i in range(n)], np.uint16)
             assert np.array_equal(ag[w][idx], src)
+
+
+# --------------------------------------------------------------------------
+# Several buckets in one fused buffer
+# --------------------------------------------------------------------------
+
+def test_bucketed_plan_matches_hand_derived_table():
+    rows, extra = [], {}
+    with open(os.path.join(GOLDEN, "bucketed_plan.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            if parts[0].isdigit():
+                rows.append(tuple(map(int, parts)))
+            else:
+                extra[parts[0]] = int(parts[1])
+    L = O.Layout([7, 5, 3], [8, 1, 4], 4, 4, bucket=[0, 0, 1])
+    assert [(p, b, int(L.o[p])) for p, b, _ in rows] == rows
+    assert L.sum_padded == extra["end"]
+    assert L.slice("f32") == extra["slice_f32"] and L.slice("bf16") == extra["slice_bf16"]
+
+
+def test_bucket_bases_are_512_byte_aligned_in_both_dtypes():
+    rng = np.random.default_rng(4)
+    d0 = [int(x) for x in rng.integers(0, 300, 20)]
+    inner = [int(x) for x in rng.choice([1, 3, 7, 64], 20)]
+    bucket = sorted(int(x) for x in rng.integers(0, 6, 20))
+    L = O.Layout(d0, inner, 8, 4, bucket=bucket)
+    for p in range(1, 20):
+        if bucket[p] != bucket[p - 1]:
+            assert L.o[p] % 256 == 0  # 512 B in bf16, 1024 B in fp32
+            assert L.o[p] - (L.o[p - 1] + L.dss[p - 1] * L.inner[p - 1]) < 256
+        else:
+            assert L.o[p] == L.o[p - 1] + L.dss[p - 1] * L.inner[p - 1]
+    with pytest.raises(O.OracleError):
+        O.Layout([4, 4], [1, 1], 4, 4, bucket=[1, 0])  # buckets must follow registration order
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_bucketed_sharded_grads_equal_dense_sum(dt):
+    # one fused sync over several buckets gives each parameter exactly what a
+    # single-bucket plan gives it (the gaps between buckets stay +0)
+    d0, inner, bucket = [13, 8, 5, 31, 2], [3, 16, 1, 2, 9], [0, 0, 1, 2, 2]
+    Lb = O.Layout(d0, inner, 8, 4, bucket=bucket)
+    L1 = O.Layout(d0, inner, 8, 4)
+    ints, grads = int_grads(L1, 77, dt)
+    fb = O.fused_from_grads(Lb, grads, dt)
+    out_b = O.apply_grads(Lb, fb, "avg", dt)
+    out_1 = O.apply_grads(L1, O.fused_from_grads(L1, grads, dt), "avg", dt)
+    assert all(np.array_equal(a, b) for a, b in zip(out_b, out_1))
+    for w in range(8):
+        data = np.zeros(Lb.slice("f32"), bool)
+        for p in range(Lb.P):
+            data[Lb.o[p]:Lb.o[p] + Lb.shard_numel(p, w % 4)] = True
+        assert (fb[w][~data] == 0).all()
+    # the forward path round-trips through bucketed slices as well
+    shards = cut_shards(Lb, grads, dt)
+    full = O.ag_copy_out(Lb, O.ag_gather(Lb, O.ag_copy_in(Lb, shards, dt, dt), dt), dt)
+    for w in range(8):
+        d = w // 4
+        for p in range(Lb.P):
+            rows = np.concatenate([shards[(d * 4 + s) * Lb.P + p] for s in range(4)])
+            assert np.array_equal(full[w * Lb.P + p], rows)
