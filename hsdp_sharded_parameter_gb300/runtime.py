@@ -102,8 +102,139 @@ class HsdpUnit:
         self.unshard(fuse_gather, stream)
         self.reduce_grads(op, stream=stream)
 
+    # unfused halves, for the pipelined backward
+    def rs(self, op="avg", stream=None):
+        """Shard-domain ReduceScatter: copy-in, then the shard-group sum."""
+        C.fsdp_rs_copy_in(self.plan, self.b_grads, self.b_rs_in, stream)
+        C.fsdp_rs_reduce(self.plan, self.b_rs_in, op, self.b_fused, stream)
+
+    def ar(self, op="avg", stream=None):
+        """Replicate-domain AllReduce of the fused buffer, in place."""
+        C.fsdp_ar_reduce(self.plan, self.b_fused, op, stream)
+
+    def capture_step(self, op="avg", fuse_gather=True, warmup=2):
+        """Records one step into a CUDA graph (after `warmup` eager steps on a
+        side stream, which also fixes every launch's grid) and returns it;
+        graph.replay() then issues the whole step with one launch."""
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                self.step(op, fuse_gather)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.step(op, fuse_gather)
+        return graph
+
     def close(self):
         for b in [self.b_shards, self.b_ag, self.b_full, self.b_grads, self.b_fused, self.b_shard_grads]:
             b.close()
         if self.rs_in is not None:
             self.b_rs_in.close()
+
+
+class BackwardPipeline:
+    """Gradient sync of a stack of HSDP units (one per layer) overlapped with
+    the backward computation, in the order of the pages' backward hook
+    ("Hyper通信掩盖方案" PR #758 write-up §二.2, the 4-step pipeline), on
+    three streams: the compute stream (the caller's current stream), a
+    shard-domain stream for ReduceScatter, a replicate-domain stream for the
+    fused AllReduce. Layers are visited last to first. After layer L's
+    gradients are produced:
+
+      step 1: the compute stream waits for layer L+1's ReduceScatter;
+      step 2: pure-FSDP layers (dp_size 1) apply their RS result at once;
+      step 3: layer L's ReduceScatter is issued on the shard stream;
+      step 4: layer L+1's fused AllReduce is issued on the replicate stream.
+
+    At the end (the root's delay_apply_reduce_grads) the compute stream
+    waits for the last ReduceScatter and every AllReduce and applies the
+    remaining layers. With fused=True each layer's RS + AR run as the single
+    fused kernel on the shard stream and are applied at the end. No call
+    blocks the host; finish() waits on the host with a time limit."""
+
+    def __init__(self, units, op="avg", fused=False):
+        self.units = list(units)
+        self.op = op
+        self.fused = fused
+        dev = self.units[0].device if self.units else torch.device("cuda")
+        self.rs_stream = torch.cuda.Stream(device=dev)
+        self.ar_stream = torch.cuda.Stream(device=dev)
+        self.log = []  # (step, layer) in issue order
+
+    def _apply(self, L, stream=None):
+        u = self.units[L]
+        # unfused results are already scaled by the collectives (AVG);
+        # the fused buffer holds the raw sum
+        op = self.op if self.fused else "sum"
+        C.fsdp_apply_grads(u.plan, u.b_fused, op, u.b_shard_grads, False, stream)
+        self.log.append(("apply", L))
+
+    def run(self, backward_compute):
+        """backward_compute(L) issues layer L's backward on the current
+        stream (it produces units[L].grads). Returns the event that marks
+        the end of the whole sync on the compute stream."""
+        comp = torch.cuda.current_stream()
+        n = len(self.units)
+        ev_rs = [None] * n
+        ev_ar = []
+        pending_apply = []
+        for L in reversed(range(n)):
+            backward_compute(L)
+            self.log.append(("compute", L))
+            ev_grad = comp.record_event()
+            prev = L + 1 if L + 1 < n else None
+            if prev is not None and not self.fused:
+                comp.wait_event(ev_rs[prev])                       # step 1
+                self.log.append(("wait_rs", prev))
+                if self.units[prev].plan.D == 1:                   # step 2
+                    self._apply(prev, comp)
+            self.rs_stream.wait_event(ev_grad)                     # step 3
+            with torch.cuda.stream(self.rs_stream):
+                if self.fused:
+                    self.units[L].rs_ar_reduce()
+                else:
+                    self.units[L].rs(self.op)
+            self.log.append(("rs", L))
+            ev_rs[L] = self.rs_stream.record_event()
+            if self.fused:
+                pending_apply.append(L)
+            elif prev is not None and self.units[prev].plan.D > 1:  # step 4
+                self.ar_stream.wait_event(ev_rs[prev])
+                with torch.cuda.stream(self.ar_stream):
+                    self.units[prev].ar(self.op)
+                self.log.append(("ar", prev))
+                ev_ar.append(self.ar_stream.record_event())
+                pending_apply.append(prev)
+        # root: the last layer visited (0) and every pending AllReduce
+        if n:
+            comp.wait_event(ev_rs[0])
+            self.log.append(("wait_rs", 0))
+            if not self.fused:
+                if self.units[0].plan.D == 1:
+                    self._apply(0, comp)
+                else:
+                    self.ar_stream.wait_event(ev_rs[0])
+                    with torch.cuda.stream(self.ar_stream):
+                        self.units[0].ar(self.op)
+                    self.log.append(("ar", 0))
+                    ev_ar.append(self.ar_stream.record_event())
+                    pending_apply.append(0)
+        for ev in ev_ar:
+            comp.wait_event(ev)
+        for L in pending_apply:
+            self._apply(L, comp)
+        return comp.record_event()
+
+    @staticmethod
+    def finish(event, timeout_s=60.0, poll_s=0.001):
+        """Waits on the host for `event` for at most timeout_s seconds;
+        raises TimeoutError instead of blocking forever."""
+        import time
+
+        deadline = time.monotonic() + timeout_s
+        while not event.query():
+            if time.monotonic() > deadline:
+                raise TimeoutError(f"gradient sync not finished after {timeout_s} s")
+            time.sleep(poll_s)
