@@ -54,6 +54,10 @@ def parse(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="scale every dim 0 (small cases for profiler captures only)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step replayed from a CUDA graph (launch-bound workloads)")
+    ap.add_argument("--pipeline", type=int, default=0, metavar="LAYERS",
+                    help="also measure the pipelined backward over LAYERS layers of the workload")
     return ap.parse_args(argv)
 
 
@@ -434,9 +438,32 @@ def run_gpu(args, wl):
                            "frac": round(ub / (us * 1e-6) / 1e9 / peak, 4),
                            "replaces_us": round(kernels["ag_copy_in"]["us"] + kernels["ag_copy_out"]["us"], 2)}
 
+    if args.graph:
+        graph = unit.capture_step()
+        ev_g = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ms_g = 0.0
+        for _ in range(ku):
+            if flush:
+                scratch.zero_()
+            ev_g[0].record(stream)
+            graph.replay()
+            ev_g[1].record(stream)
+            torch.cuda.synchronize()
+            ms_g += ev_g[0].elapsed_time(ev_g[1])
+        extra["graph_step"] = {"us": round(ms_g / ku * 1e3, 2),
+                               "eager_us": round(sum(kernels[n]["us"] for n in KERNELS), 2)}
+        del graph
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, unit, calls, step_bytes, world, dev)
+
+    pipeline = None
+    if args.pipeline:
+        unit.close()
+        del unit
+        torch.cuda.empty_cache()
+        pipeline = run_pipeline(args, wl, d0, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -457,9 +484,74 @@ def run_gpu(args, wl):
                 "kernels": kernels, "kernels_outside_step": extra,
                 "roofline": roofline, "roofline_second": roofline_2,
                 "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches}
+        if pipeline:
+            line["pipeline"] = pipeline
         print(json.dumps(line), flush=True)
-    unit.close()
+    if not args.pipeline:
+        unit.close()
     return 0
+
+
+def run_pipeline(args, wl, d0, dev):
+    """Overlap of the gradient sync with backward compute over a stack of
+    layers: the stand-in backward of a layer is bf16 GEMMs on the compute
+    stream sized to take about as long as that layer's sync; the sync runs
+    the pages' 4-step pipeline (unfused) or the fused kernel per layer."""
+    import torch
+
+    from hsdp_sharded_parameter_gb300 import capi as C
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+    from hsdp_sharded_parameter_gb300.runtime import BackwardPipeline, HsdpUnit
+
+    n = args.pipeline
+    units = []
+    for i in range(n):
+        u = HsdpUnit(C.Plan(d0, wl.inner, wl.rank_size, wl.shard_size).upload(), wl.param_dtype,
+                     wl.grad_dtype, device=dev, with_unfused=True)
+        WL.torch_fill_(u.grads, wl.seed_grads + 100 * i, wl.grad_std, wl.grad_dtype)
+        units.append(u)
+    a = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    comp = torch.cuda.current_stream()
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(comp)
+        for _ in range(reps):
+            fn()
+        e.record(comp)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    # size the stand-in backward of one layer to about one layer's fused sync
+    t_sync1 = timed(lambda: units[0].reduce_grads("avg"))
+    t_mm = timed(lambda: torch.mm(a, a))
+    k = max(1, int(round(t_sync1 / t_mm)))
+
+    def compute(L):
+        for _ in range(k):
+            torch.mm(a, a)
+
+    out = {"layers": n, "workload": wl.key, "gemms_per_layer": k, "gemm": "8192^3 bf16"}
+    t_comp = timed(lambda: [compute(L) for L in reversed(range(n))])
+    out["compute_only_ms"] = round(t_comp, 3)
+    for fused in (True, False):
+        name = "fused" if fused else "unfused_4step"
+        if fused:
+            t_sync = timed(lambda: [units[L].reduce_grads("avg") for L in reversed(range(n))])
+        else:
+            t_sync = timed(lambda: [units[L].reduce_grads_unfused("avg") for L in reversed(range(n))])
+        res = {"sync_only_ms": round(t_sync, 3), "serial_ms": round(t_comp + t_sync, 3)}
+        # sync kernels on the whole GPU (0) or on a capped number of blocks
+        for cap in (0, 32, 64, 128):
+            t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap).run(compute))
+            hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
+            res[f"comm_blocks_{cap}"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
+        out[name] = res
+    for u in units:
+        u.close()
+    return out
 
 
 def run_e2e(args, unit, calls, step_bytes, world, dev):

@@ -65,6 +65,7 @@ def lib():
         L.fsdp_plan_create_bucketed.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, P(vp)]
         L.fsdp_plan_destroy.argtypes = [vp]
         L.fsdp_plan_upload.argtypes = [vp]
+        L.fsdp_plan_set_grid_limit.argtypes = [vp, i32]
         L.fsdp_plan_info.argtypes = [vp, P(i32), P(i32), P(i32), P(i32), P(i64)]
         L.fsdp_slice_numel.argtypes = [vp, i32, P(i64)]
         L.fsdp_sharded_size.argtypes = [vp, i32, i32, P(i64), P(i64)]
@@ -142,6 +143,10 @@ class Plan:
 
     def upload(self):
         _check(lib().fsdp_plan_upload(self.handle))
+        return self
+
+    def set_grid_limit(self, max_blocks):
+        _check(lib().fsdp_plan_set_grid_limit(self.handle, int(max_blocks)))
         return self
 
     def slice_numel(self, dt):

@@ -212,6 +212,7 @@ KArgs base_args(const fsdp_plan_s* pl, TableId t, int reps) {
     a.S = pl->S;
     a.D = pl->D;
     a.W = pl->W;
+    a.max_grid = pl->max_grid;
     set_divisor(a, 1);
     return a;
 }
@@ -349,6 +350,14 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
     }
     pl->device = dev;
     pl->uploaded = true;
+    return FSDP_OK;
+}
+
+int fsdp_plan_set_grid_limit(fsdp_plan_t pl, int max_blocks) {
+    clear_error();
+    FSDP_CHECK_PLAN(pl);
+    if (max_blocks < 0) return set_error(FSDP_ERR_INVALID_ARG, "plan_set_grid_limit: max_blocks must be >= 0");
+    pl->max_grid = max_blocks;
     return FSDP_OK;
 }
 

@@ -90,6 +90,7 @@ struct KArgs {
     // agree bit for bit, subnormals included); 2 = IEEE division.
     int scale_mode;
     float recip;
+    int max_grid;  // upper bound on the launch's blocks (0 = one persistent wave)
 };
 
 // Fills div, scale_mode and recip for a divisor d >= 1.
@@ -123,6 +124,7 @@ struct fsdp_plan_s {
     int64_t sum_padded = 0;
     int device = -1;
     bool uploaded = false;
+    int max_grid = 0;  // fsdp_plan_set_grid_limit
     void* dev_block = nullptr;
     fsdp::Table tables[fsdp::T_COUNT];
     int64_t slice(int dt) const {

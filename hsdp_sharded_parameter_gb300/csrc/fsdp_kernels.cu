@@ -1050,7 +1050,8 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     const int per_sm = blocks_per_sm(fn, threads, smem);
     const int64_t warps = a.ntiles * a.reps;
     const int64_t want = (warps + threads / 32 - 1) / (threads / 32);
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    int64_t cap = (int64_t)sm_count() * per_sm;
+    if (a.max_grid > 0 && a.max_grid < cap) cap = a.max_grid;
     const int grid = (int)(want < cap ? want : cap);
     kernel<<<grid, threads, smem, st>>>(a);
     return cudaGetLastError();

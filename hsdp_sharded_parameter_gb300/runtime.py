@@ -154,13 +154,18 @@ class BackwardPipeline:
     fused kernel on the shard stream and are applied at the end. No call
     blocks the host; finish() waits on the host with a time limit."""
 
-    def __init__(self, units, op="avg", fused=False):
+    def __init__(self, units, op="avg", fused=False, comm_blocks=0):
+        """comm_blocks > 0 caps the thread blocks of every sync kernel the
+        pipeline issues (fsdp_plan_set_grid_limit), leaving the other SMs to
+        the backward compute; the sync streams get high priority so their
+        blocks are placed as soon as SMs free up."""
         self.units = list(units)
         self.op = op
         self.fused = fused
+        self.comm_blocks = comm_blocks
         dev = self.units[0].device if self.units else torch.device("cuda")
-        self.rs_stream = torch.cuda.Stream(device=dev)
-        self.ar_stream = torch.cuda.Stream(device=dev)
+        self.rs_stream = torch.cuda.Stream(device=dev, priority=-1)
+        self.ar_stream = torch.cuda.Stream(device=dev, priority=-1)
         self.log = []  # (step, layer) in issue order
 
     def _apply(self, L, stream=None):
@@ -175,6 +180,15 @@ class BackwardPipeline:
         """backward_compute(L) issues layer L's backward on the current
         stream (it produces units[L].grads). Returns the event that marks
         the end of the whole sync on the compute stream."""
+        for u in self.units:
+            u.plan.set_grid_limit(self.comm_blocks)
+        try:
+            return self._run(backward_compute)
+        finally:
+            for u in self.units:
+                u.plan.set_grid_limit(0)
+
+    def _run(self, backward_compute):
         comp = torch.cuda.current_stream()
         n = len(self.units)
         ev_rs = [None] * n

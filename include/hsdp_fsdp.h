@@ -139,6 +139,15 @@ int fsdp_plan_destroy(fsdp_plan_t plan);
  * must then run with that device current. Calling it again is a no-op. */
 int fsdp_plan_upload(fsdp_plan_t plan);
 
+/* Caps the number of thread blocks every later data call of this plan
+ * launches (0, the default: one persistent wave over the whole GPU). The
+ * kernels stride over their work, so any cap gives the same results; a
+ * small cap leaves the other SMs to kernels running beside them, e.g. the
+ * backward compute the gradient sync overlaps with, the way the pages'
+ * communication streams run beside compute [OVERLAP §二.2]. May be changed
+ * between calls. */
+int fsdp_plan_set_grid_limit(fsdp_plan_t plan, int max_blocks);
+
 /* Mesh sizes and the unpadded total sum_p chunk_p * inner_p. Any output
  * pointer may be NULL. */
 int fsdp_plan_info(fsdp_plan_t plan, int* rank_size, int* shard_size, int* dp_size,
