@@ -104,9 +104,20 @@ def dist_sum(value, world, device="cpu"):
 
 def barrier(world):
     if world > 1:
+        import torch
         import torch.distributed as dist
 
-        dist.barrier()
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def host_memory_bytes():
+    try:
+        return os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
 
 
 # --------------------------------------------------------------------------
@@ -563,6 +574,13 @@ def run_e2e(args, unit, calls, step_bytes, world, dev):
 
     ins = unit.shards + unit.grads
     outs = unit.full + unit.shard_grads
+    need = sum(t.numel() * t.element_size() for t in ins + outs)
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    have = host_memory_bytes()
+    if have and need * local_ranks > 0.6 * have:
+        # pinned host copies of every rank's inputs and outputs would not fit
+        return {"skipped": f"pinned host buffers need {need * local_ranks / 1e9:.0f} GB for "
+                           f"{local_ranks} local ranks, host has {have / 1e9:.0f} GB"}
     h_in = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True) for t in ins]
     h_out = [torch.empty(t.numel(), dtype=t.dtype, pin_memory=True) for t in outs]
     for h, t in zip(h_in, ins):
