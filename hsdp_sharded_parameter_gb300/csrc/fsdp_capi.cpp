@@ -213,6 +213,7 @@ KArgs base_args(const fsdp_plan_s* pl, TableId t, int reps) {
     a.D = pl->D;
     a.W = pl->W;
     a.max_grid = pl->max_grid;
+    a.staged_blocks = pl->staged_blocks;
     set_divisor(a, 1);
     return a;
 }
@@ -320,6 +321,18 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
     std::vector<Seg> segs[T_COUNT];
     std::vector<int64_t> tiles[T_COUNT];
     build_tables(*pl, segs, tiles);
+    // Share of the fused region's data in runs whose bf16 source is shifted
+    // against the fp32 destination's 16-byte grid (16-byte aligned buffers
+    // assumed): picks the staged reduce's blocks per SM.
+    {
+        int64_t shifted = 0, total = 0;
+        for (const Seg& g : segs[T_RSAR]) {
+            if (g.p < 0) continue;
+            total += g.n;
+            if ((((g.src_off - (g.dst_off & 3)) * 2) & 15) != 0) shifted += g.n;
+        }
+        pl->staged_blocks = 2 * shifted > total ? 3 : 2;
+    }
     size_t bytes = 0;
     size_t seg_at[T_COUNT], tile_at[T_COUNT];
     for (int t = 0; t < T_COUNT; ++t) {
@@ -525,6 +538,7 @@ int fsdp_ag_gather(fsdp_plan_t pl, fsdp_binding_t ag_out, fsdp_stream_t stream) 
     a.src_tab = ag_out->dev_table;
     a.dst_tab = ag_out->dev_table;
     a.vec = ag_out->aligned16;
+    a.dests = pl->S - 1;
     return run(K_GATHER, ag_out->dt, ag_out->dt, a, stream, "ag_gather");
 }
 

@@ -91,6 +91,12 @@ struct KArgs {
     int scale_mode;
     float recip;
     int max_grid;  // upper bound on the launch's blocks (0 = one persistent wave)
+    // Blocks per SM for the staged reduce (0 = as many as fit): 2 when most
+    // of the fused region's data sits in runs aligned with their sources,
+    // 3 when most runs are shifted (their steps do more work per byte, so
+    // more warps are needed to keep the same bytes in flight).
+    int staged_blocks;
+    int dests;  // destinations written per tile when more than one (the gather)
 };
 
 // Fills div, scale_mode and recip for a divisor d >= 1.
@@ -125,6 +131,7 @@ struct fsdp_plan_s {
     int device = -1;
     bool uploaded = false;
     int max_grid = 0;  // fsdp_plan_set_grid_limit
+    int staged_blocks = 2;  // see KArgs::staged_blocks, set by fsdp_plan_upload
     void* dev_block = nullptr;
     fsdp::Table tables[fsdp::T_COUNT];
     int64_t slice(int dt) const {

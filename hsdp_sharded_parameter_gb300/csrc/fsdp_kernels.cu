@@ -241,17 +241,26 @@ __device__ __forceinline__ void copy_elem(D* dst, int64_t di, const S* src, int6
 // ----------------------------------------------------------- work search
 
 // Largest k with tb[k] <= tile, searching forward from k (tb strictly
-// increasing, tb[nseg] > tile). Warp-uniform; all 32 lanes take part.
+// increasing, tb[k] <= tile < tb[nseg]). Warp-uniform; all 32 lanes take
+// part. The common case (same or next run) costs one or two loads; a longer
+// jump narrows [lo, hi) 32-fold per round: lane i probes lo + i*step and a
+// ballot counts the probes at or below the tile (they form a prefix).
 __device__ __forceinline__ int find_seg(const int64_t* __restrict__ tb, int nseg, int k, int64_t tile) {
     if (tile < __ldg(tb + k + 1)) return k;
+    if (k + 2 > nseg || tile < __ldg(tb + k + 2)) return k + 1;
     const int lane = threadIdx.x & 31;
-    for (;;) {
-        const int idx = k + 1 + lane;
-        const bool le = idx < nseg && __ldg(tb + idx) <= tile;
-        const unsigned m = __ballot_sync(kFull, le);
-        if (m != kFull) return k + __popc(m);
-        k += 32;
+    int lo = k + 1, hi = nseg;  // tb[lo] <= tile < tb[hi]
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int idx = lo + lane * step;
+        const bool le = idx < hi && __ldg(tb + idx) <= tile;
+        const int c = __popc(__ballot_sync(kFull, le));  // >= 1: lane 0 probes lo
+        const int nlo = lo + (c - 1) * step;
+        const int nhi = lo + c * step;
+        lo = nlo;
+        hi = nhi < hi ? nhi : hi;
     }
+    return lo;
 }
 
 // One warp tile: a window of up to kWarpTile elements of one run. rel0 is
@@ -1043,12 +1052,45 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
     return b;
 }
 
+// Blocks per SM of each kernel family's grid: 0 = as many as fit at once
+// (one persistent wave). DRAM throughput depends on how many warps stream
+// at the same time, not monotonically, so each family has its own value,
+// chosen by a sweep on the large HSDP layer (a value above what fits gives
+// several waves; each warp still strides over the whole table):
+//   copy-out 16 (0.955 -> 1.006 of the measured copy peak), fused copy-in
+//   32 (0.889 -> 0.998), apply 16 (0.967 -> 0.992); the direct unshard was
+//   best at one wave. The staged reduce takes KArgs::staged_blocks, which
+//   the plan derives from its layout (0 here = use that hint).
+#ifndef FSDP_GRID_COPY
+#define FSDP_GRID_COPY 16
+#endif
+#ifndef FSDP_GRID_MULTI
+#define FSDP_GRID_MULTI 32
+#endif
+#ifndef FSDP_GRID_APPLY
+#define FSDP_GRID_APPLY 16
+#endif
+#ifndef FSDP_GRID_STAGED
+#define FSDP_GRID_STAGED 0
+#endif
+#ifndef FSDP_GRID_UNSHARD
+#define FSDP_GRID_UNSHARD 0
+#endif
+
 template <typename F>
-cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0) {
+cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0,
+               int grid_per_sm = 0) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     sm_count();
-    const int per_sm = blocks_per_sm(fn, threads, smem);
+    const int resident = blocks_per_sm(fn, threads, smem);  // also raises the smem limit once
     const int64_t warps = a.ntiles * a.reps;
+    int per_sm = grid_per_sm > 0 ? grid_per_sm : resident;
+    // Several waves pay off only for long launches; a launch with fewer than
+    // 100 tiles per resident warp (many small runs) stays at one wave. A
+    // tile written to several destinations counts once per destination.
+    const int64_t dests = a.fuse ? a.S : (a.dests > 1 ? a.dests : 1);
+    if (per_sm > resident && warps * dests < (int64_t)resident * sm_count() * (threads / 32) * 100)
+        per_sm = resident;
     const int64_t want = (warps + threads / 32 - 1) / (threads / 32);
     int64_t cap = (int64_t)sm_count() * per_sm;
     if (a.max_grid > 0 && a.max_grid < cap) cap = a.max_grid;
@@ -1059,7 +1101,8 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
 
 template <typename S, typename F>
 cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd) {
-    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * Staging<S>::warp_bytes(ns, nd));
+    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * Staging<S>::warp_bytes(ns, nd),
+              FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks);
 }
 
 // The staged reduce fits when its per-block shared memory stays well inside
@@ -1078,16 +1121,18 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
         case K_AGIN:
             if (sf && df) return go(ag_copy_in_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
             if (sf) return go(ag_copy_in_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
-            return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+            return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
+                      FSDP_GRID_MULTI);
         case K_GATHER:
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
                       : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
         case K_UNSHARD:
             if (sf && df) return go(ag_unshard_kernel<float, float>, a, st);
             if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st);
-            return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st);
+            return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st, kThreads, 0, FSDP_GRID_UNSHARD);
         case K_AGOUT:
-            return sf ? go(ag_copy_out_kernel<float>, a, st) : go(ag_copy_out_kernel<uint16_t>, a, st);
+            return sf ? go(ag_copy_out_kernel<float>, a, st)
+                      : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
         case K_RSIN:
             return sf ? go(rs_copy_in_kernel<float>, a, st) : go(rs_copy_in_kernel<uint16_t>, a, st);
         case K_RSAR:
@@ -1118,7 +1163,8 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             if (a.D == 8) return go_staged<float>(ar_reduce_kernel<8>, a, st, 8, 8);
             return go_staged<float>(ar_reduce_kernel<0>, a, st, a.D, a.D);
         case K_APPLY:
-            return df ? go(apply_grads_kernel<float>, a, st) : go(apply_grads_kernel<uint16_t>, a, st);
+            return df ? go(apply_grads_kernel<float>, a, st)
+                      : go(apply_grads_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_APPLY);
     }
     return cudaErrorInvalidValue;
 }
