@@ -565,7 +565,10 @@ int fsdp_ag_unshard(fsdp_plan_t pl, fsdp_binding_t shards, fsdp_binding_t full, 
     if ((rc = check_binding(pl, full, FSDP_ROLE_FULL_PARAMS, "ag_unshard"))) return rc;
     if (shards->dt == FSDP_BF16 && full->dt == FSDP_F32)
         return set_error(FSDP_ERR_INVALID_ARG, "ag_unshard: bf16 shards cannot be gathered as f32");
-    KArgs a = base_args(pl, full->dt == FSDP_F32 ? T_UNSHARD_F32 : T_UNSHARD_BF16, pl->W);
+    // one repetition per replica: each shard tile is read once and written
+    // to every shard-group member's full parameter
+    KArgs a = base_args(pl, full->dt == FSDP_F32 ? T_UNSHARD_F32 : T_UNSHARD_BF16, pl->D);
+    a.dests = pl->S;
     a.src_tab = shards->dev_table;
     a.dst_tab = full->dev_table;
     a.vec = full->aligned16;

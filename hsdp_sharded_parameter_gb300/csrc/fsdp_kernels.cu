@@ -302,7 +302,7 @@ __device__ __forceinline__ const S* copy_src(const KArgs& a, const Tile& ti) {
     if (KIND == K_GATHER) return static_cast<const S*>(a.src_tab[ti.rep * a.S + ti.row]);
     if (KIND == K_AGOUT) return static_cast<const S*>(a.src_tab[ti.rep]);
     if (KIND == K_UNSHARD)
-        return static_cast<const S*>(a.src_tab[(int64_t)((ti.rep / a.S) * a.S + ti.row) * a.P + ti.p]);
+        return static_cast<const S*>(a.src_tab[(int64_t)(ti.rep * a.S + ti.row) * a.P + ti.p]);
     return ti.p >= 0 ? static_cast<const S*>(a.src_tab[(int64_t)ti.rep * a.P + ti.p]) : nullptr;
 }
 
@@ -310,6 +310,7 @@ template <int KIND>
 __device__ __forceinline__ int copy_ndst(const KArgs& a) {
     if (KIND == K_AGIN) return a.fuse ? a.S : 1;
     if (KIND == K_GATHER) return a.S - 1;
+    if (KIND == K_UNSHARD) return a.S;
     return 1;
 }
 
@@ -320,8 +321,10 @@ __device__ __forceinline__ D* copy_dst(const KArgs& a, const Tile& ti, int j) {
         d = static_cast<D*>(a.dst_tab[ti.rep * a.S + (a.fuse ? j : ti.row)]);
     else if (KIND == K_GATHER)
         d = static_cast<D*>(a.dst_tab[ti.rep * a.S + j + (j >= ti.row ? 1 : 0)]);
-    else if (KIND == K_AGOUT || KIND == K_UNSHARD)
+    else if (KIND == K_AGOUT)
         d = static_cast<D*>(a.dst_tab[(int64_t)ti.rep * a.P + ti.p]);
+    else if (KIND == K_UNSHARD)  // shard-group member j of replica rep
+        d = static_cast<D*>(a.dst_tab[(int64_t)(ti.rep * a.S + j) * a.P + ti.p]);
     else
         d = static_cast<D*>(a.dst_tab[ti.rep]);
     return d + ti.dst_off;
@@ -983,7 +986,7 @@ __global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, false>(a); }
+__global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
 template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
@@ -1058,8 +1061,8 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 // chosen by a sweep on the large HSDP layer (a value above what fits gives
 // several waves; each warp still strides over the whole table):
 //   copy-out 16 (0.955 -> 1.006 of the measured copy peak), fused copy-in
-//   32 (0.889 -> 0.998), apply 16 (0.967 -> 0.992); the direct unshard was
-//   best at one wave. The staged reduce takes KArgs::staged_blocks, which
+//   32 (0.889 -> 0.998), apply 16 (0.967 -> 0.992), direct unshard 32
+//   (0.90 -> 0.999). The staged reduce takes KArgs::staged_blocks, which
 //   the plan derives from its layout (0 here = use that hint).
 #ifndef FSDP_GRID_COPY
 #define FSDP_GRID_COPY 16
@@ -1074,7 +1077,7 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #define FSDP_GRID_STAGED 0
 #endif
 #ifndef FSDP_GRID_UNSHARD
-#define FSDP_GRID_UNSHARD 0
+#define FSDP_GRID_UNSHARD 32
 #endif
 
 template <typename F>
@@ -1127,9 +1130,10 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
                       : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
         case K_UNSHARD:
-            if (sf && df) return go(ag_unshard_kernel<float, float>, a, st);
-            if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st);
-            return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st, kThreads, 0, FSDP_GRID_UNSHARD);
+            if (sf && df) return go(ag_unshard_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
+            if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+            return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
+                      FSDP_GRID_UNSHARD);
         case K_AGOUT:
             return sf ? go(ag_copy_out_kernel<float>, a, st)
                       : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
