@@ -418,9 +418,8 @@ def run_gpu(args, wl):
 
     # Not part of the step: the direct unshard (all three forward steps in
     # one pass, no gathered buffer), timed alone on the same unit. It reads
-    # each shard from DRAM once (the shard-group members read the same tile
-    # within a few warps of each other, so repeats come from L2) and writes
-    # every rank's full parameters.
+    # each shard once and writes it into every shard-group member's full
+    # parameter.
     extra = {}
     ev_u = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     for _ in range(2):

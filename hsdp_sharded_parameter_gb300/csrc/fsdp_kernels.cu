@@ -5,19 +5,23 @@
 //   * A plan-time table lists runs ("segments") of contiguous elements; a
 //     prefix array gives each run's first warp tile (2048 elements: 8 steps
 //     of 32 lanes x 8 elements).
-//   * A persistent grid of warps strides over (tile, repetition) pairs,
-//     repetition fastest (the ranks or replicas the table is repeated for).
-//     A warp finds its run with a cooperative forward search (each lane
-//     tests one tile boundary; a ballot picks the run), so the cursor only
-//     moves forward; the next tile's run is looked up while the current
-//     tile's loads are in flight.
+//   * A grid of warps strides over (tile, repetition) pairs, repetition
+//     fastest (the ranks or replicas the table is repeated for); each kernel
+//     family has its own measured grid size (see FSDP_GRID_*). A warp finds
+//     its run with a cooperative search over the prefix array (a ballot over
+//     32 probes narrows the range 32-fold per round), moving only forward;
+//     the next tile's run is looked up while the current tile's loads are in
+//     flight.
 //   * Granules are anchored at 16-byte boundaries of the destination, so
 //     every full granule is written with aligned 16-byte stores. Partial
 //     granules (run heads/tails) and destinations that are not 16-byte
 //     aligned go element by element.
 //   * Copy kernels read with aligned 16-byte loads into registers; a source
-//     run shifted against its destination (ragged offsets) is realigned by
-//     loading the two aligned blocks around each granule and funnel-shifting.
+//     run shifted against its destination (ragged offsets) is realigned with
+//     funnel shifts, each lane taking its neighbour block from the next lane
+//     by a warp shuffle. Kernels that write one tile to several destinations
+//     (fused copy-in, gather, direct unshard) stage it in shared memory once
+//     and fan it out with TMA bulk stores.
 //   * Reduce kernels (W sources per output) stage each warp step's source
 //     windows in shared memory with cp.async (16-byte copies, one aligned
 //     window per source, one block wider when shifted) two steps deep, so
