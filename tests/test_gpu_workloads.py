@@ -198,6 +198,45 @@ def test_pure_tp_sum_op():
     free(unit, plan)
 
 
+def test_offsets_beyond_32_bits():
+    # Maximum sizes: a 600001 x 4096 bf16 parameter (2.46e9 elements, 4.9 GB
+    # per full tensor) on a (2,2) mesh, ragged over the shard group, followed
+    # by small parameters whose runs sit past 2^31 elements and 2^32 bytes in
+    # the gathered buffer, the RS input and the fp32 fused region (an inner-1
+    # parameter of odd size shifts every later run off the 16-byte grid).
+    shapes = [(600001, 4096), (5,), (9, 4096), (3,)]
+    d0 = [s[0] for s in shapes]
+    inner = [s[1] if len(s) > 1 else 1 for s in shapes]
+    plan = C.Plan(d0, inner, 4, 2).upload()
+    L = O.Layout(d0, inner, 4, 2)
+    assert 2 * L.slice("bf16") > 2**31 and L.slice("f32") * 4 > 2**32
+    unit = HsdpUnit(plan, "bf16", "bf16", with_unfused=True)
+    fill_(unit.shards, 6001, 1.0, "bf16")
+    fill_(unit.grads, 6002, 1.0, "bf16")
+    for bufs in [unit.ag_out, unit.full, unit.fused, unit.shard_grads, unit.rs_in]:
+        dirty(bufs)
+    unit.step(op="avg", fuse_gather=True)
+    torch.cuda.synchronize()
+    check_forward(L, unit)
+    check_backward(L, unit, np.random.default_rng(6003), "avg")
+    # the unfused path and the direct unshard give the same bits
+    fused = [t.clone() for t in unit.shard_grads]
+    dirty(unit.shard_grads)
+    unit.reduce_grads_unfused("avg")
+    torch.cuda.synchronize()
+    for a, b in zip(fused, unit.shard_grads):
+        assert torch.equal(bits(a), bits(b))
+    del fused
+    full = [t.clone() for t in unit.full]
+    dirty(unit.full)
+    unit.unshard_direct()
+    torch.cuda.synchronize()
+    for a, b in zip(full, unit.full):
+        assert torch.equal(bits(a), bits(b))
+    del full
+    free(unit, plan)
+
+
 def test_fused_equals_unfused_at_full_size():
     # "Hyper通信掩盖方案" PR #758 §三: comm_fusion on/off give bitwise-equal
     # gradients on the HSDP (2,4) mesh.
