@@ -128,10 +128,11 @@ __device__ __forceinline__ void load_raw_at(Raw<T>& r, uintptr_t a) {
 // All kSteps steps of an interior tile are loaded first and shuffled after:
 // a warp-synchronous shuffle keeps later loads from being issued ahead of
 // it, so interleaving them would expose one memory latency per step. step
-// is the byte distance between consecutive steps' windows.
+// is the byte distance between consecutive steps' windows. Only the first
+// nsteps steps (warp-uniform) are loaded.
 template <typename T>
 __device__ __forceinline__ void load_tile_shifted(Raw<T> (&r)[kSteps], uintptr_t w0, uintptr_t step,
-                                                  unsigned sh, int lane) {
+                                                  unsigned sh, int lane, int nsteps) {
     constexpr int kV = Raw<T>::kVec;
     uint4 blk[kSteps][kV];
     uint4 last[kSteps];
@@ -139,8 +140,8 @@ __device__ __forceinline__ void load_tile_shifted(Raw<T> (&r)[kSteps], uintptr_t
     for (int u = 0; u < kSteps; ++u) {
         const uint4* q = reinterpret_cast<const uint4*>(w0 + u * step) + lane * kV;
 #pragma unroll
-        for (int v = 0; v < kV; ++v) blk[u][v] = ld_stream(q + v);
-        last[u] = lane == 31 ? ld_stream(q + kV) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < kV; ++v) blk[u][v] = u < nsteps ? ld_stream(q + v) : make_uint4(0, 0, 0, 0);
+        last[u] = lane == 31 && u < nsteps ? ld_stream(q + kV) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kSteps; ++u) {
@@ -372,8 +373,13 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
         const int64_t tn = t + stride;
         const S* src = copy_src<KIND, S>(a, cur);
         Tile nxt;
-        if (a.vec && cur.rel0 >= 0 && cur.rel0 + kWarpTile <= cur.n) {
-            // interior tile: every granule full, destination aligned
+        // whole steps of the run from lane 0's first granule on (a short
+        // run, or a run's last tile, whose length is a multiple of a step
+        // also takes the interior path with fewer steps)
+        const int64_t ext = cur.n - cur.rel0;
+        const int nsteps = ext >= kWarpTile ? kSteps : (int)(ext / kStepElems);
+        if (a.vec && cur.rel0 >= 0 && (ext >= kWarpTile || ext % kStepElems == 0)) {
+            // interior tile: nsteps steps, every granule full, destination aligned
             Raw<D> val[kSteps];
             if (src == nullptr) {
 #pragma unroll
@@ -386,12 +392,15 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
 #pragma unroll
                     for (int u = 0; u < kSteps; ++u) {
                         Raw<S> r;
-                        load_raw_at(r, b + (uintptr_t)(u * kStepElems * (int)sizeof(S)));
+                        if (u < nsteps)
+                            load_raw_at(r, b + (uintptr_t)(u * kStepElems * (int)sizeof(S)));
+                        else
+                            zero_raw(r);
                         convert(r, val[u]);
                     }
                 } else {
                     Raw<S> r[kSteps];
-                    load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * (int)sizeof(S)), sh, lane);
+                    load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * (int)sizeof(S)), sh, lane, nsteps);
 #pragma unroll
                     for (int u = 0; u < kSteps; ++u) convert(r[u], val[u]);
                 }
@@ -409,14 +418,16 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
                 for (int u = 0; u < kSteps; ++u)
 #pragma unroll
                     for (int v = 0; v < Raw<D>::kVec; ++v)
-                        img[(u * 32 + lane) * Raw<D>::kVec + v] =
-                            make_uint4(val[u].w[4 * v], val[u].w[4 * v + 1], val[u].w[4 * v + 2], val[u].w[4 * v + 3]);
+                        if (u < nsteps)
+                            img[(u * 32 + lane) * Raw<D>::kVec + v] = make_uint4(
+                                val[u].w[4 * v], val[u].w[4 * v + 1], val[u].w[4 * v + 2], val[u].w[4 * v + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(img));
                     for (int j = 0; j < nd; ++j)
-                        bulk_store(copy_dst<KIND, D>(a, cur, j) + cur.rel0, s, kWarpTile * (uint32_t)sizeof(D));
+                        bulk_store(copy_dst<KIND, D>(a, cur, j) + cur.rel0, s,
+                                   (uint32_t)(nsteps * kStepElems) * (uint32_t)sizeof(D));
                     bulk_commit();
                 }
                 parity ^= 1;
@@ -424,7 +435,8 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
                 for (int j = 0; j < nd; ++j) {
                     D* d = copy_dst<KIND, D>(a, cur, j) + cur.rel0 + lane * kGran;
 #pragma unroll
-                    for (int u = 0; u < kSteps; ++u) store_raw(d + u * kStepElems, val[u]);
+                    for (int u = 0; u < kSteps; ++u)
+                        if (u < nsteps) store_raw(d + u * kStepElems, val[u]);
                 }
             }
         } else {
@@ -517,7 +529,7 @@ __device__ __forceinline__ void apply_body(const KArgs& a) {
 #pragma unroll
                 for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
             } else {
-                load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * 4), sh, lane);
+                load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * 4), sh, lane, kSteps);
             }
             if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
 #pragma unroll
