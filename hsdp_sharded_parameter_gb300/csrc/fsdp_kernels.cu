@@ -47,6 +47,13 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxStagedSources = 32;
+// The fused reduce fans a step's result out with TMA bulk stores (one
+// shared-memory image, one bulk store per destination) when it has at least
+// this many destinations (replicas); below, each lane stores its granule.
+constexpr int kFanOutDests = 4;
+constexpr size_t kFanImgBytes = kStepElems * sizeof(float);  // one step of fp32
+template <int KIND, int ND>
+__host__ __device__ constexpr bool fan_out() { return KIND == K_RSAR && ND >= kFanOutDests; }
 // Resident blocks of the staged reduce its shared memory allows for 16 bf16
 // sources (69 KB each); telling the compiler so lets it keep the unrolled
 // fold in registers (up to 170 each) instead of spilling.
@@ -813,7 +820,7 @@ __device__ __forceinline__ void fold_fast(const uint4* win, int lane, unsigned s
 
 template <int KIND, typename S, int NS, int SIN, int ND>
 __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, const char* stage,
-                                             const Shape<KIND, NS, SIN, ND>& sh) {
+                                             const Shape<KIND, NS, SIN, ND>& sh, uint4* img, int& parity) {
     if (!st.valid) return;
     const int lane = threadIdx.x & 31;
     const uint4* win = reinterpret_cast<const uint4*>(stage);
@@ -833,6 +840,26 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
         }
         Raw<float> o;
         narrow(total, o);
+        if (fan_out<KIND, ND>()) {
+            // the step's 256 results as one image (two per warp, in turn;
+            // an image is rewritten only after the bulk stores of two fast
+            // steps ago have read it), written to every replica by lane 0
+            uint4* im = img + parity * (int)(kFanImgBytes / 16);
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+            im[2 * lane] = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+            im[2 * lane + 1] = make_uint4(o.w[4], o.w[5], o.w[6], o.w[7]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(im));
+#pragma unroll
+                for (int j = 0; j < sh.nd; ++j) bulk_store(dp[j] + st.rel, s, (uint32_t)kFanImgBytes);
+                bulk_commit();
+            }
+            parity ^= 1;
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
         return;
@@ -900,8 +927,12 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
     extern __shared__ __align__(16) char smem_raw[];
     const Shape<KIND, NS, SIN, ND> sh(a);
     const size_t sb = Staging<S>::stage_bytes(sh.ns, sh.nd);
-    char* here = smem_raw + (threadIdx.x >> 5) * 2 * sb;  // stage of the step being folded
-    char* there = here + sb;                                 // stage of the step in flight
+    constexpr bool kFan = fan_out<KIND, ND>();
+    char* base = smem_raw + (threadIdx.x >> 5) * (2 * sb + (kFan ? 2 * kFanImgBytes : 0));
+    char* here = base;        // stage of the step being folded
+    char* there = base + sb;  // stage of the step in flight
+    uint4* img = kFan ? reinterpret_cast<uint4*>(base + 2 * sb) : nullptr;  // fan-out images
+    int parity = 0;
     StepGen gen;
     gen.init(a);
     Step cur = gen.next(a);
@@ -911,7 +942,7 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
         stage_step<KIND, S>(a, nxt, there, sh);
         cp_async_wait1();
         __syncwarp();
-        consume_step<KIND, S>(a, cur, here, sh);
+        consume_step<KIND, S>(a, cur, here, sh, img, parity);
         __syncwarp();
         cur = nxt;
         char* t = here;
@@ -919,6 +950,8 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
         there = t;
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
+    // bulk stores still reading the images or writing must finish
+    if (kFan && (threadIdx.x & 31) == 0) bulk_wait_all();
 }
 
 // Register path for more than kMaxStagedSources sources: each lane loads
@@ -1119,8 +1152,9 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
 }
 
 template <typename S, typename F>
-cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd) {
-    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * Staging<S>::warp_bytes(ns, nd),
+cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan = false) {
+    const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * kFanImgBytes : 0);
+    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp,
               FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks);
 }
 
@@ -1164,7 +1198,8 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             if (!staged_fits<uint16_t>(a.W, a.D)) return go(rs_ar_reduce_wide_kernel<uint16_t>, a, st);
 #define FSDP_RSAR(W_, S_)                                                                               \
     if (a.W == W_ && a.S == S_)                                                                         \
-        return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, W_ / S_);
+        return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, W_ / S_, \
+                                   fan_out<K_RSAR, W_ / S_>());
             FSDP_RSAR(16, 8) FSDP_RSAR(8, 4) FSDP_RSAR(8, 8) FSDP_RSAR(8, 1) FSDP_RSAR(16, 16)
             FSDP_RSAR(16, 4) FSDP_RSAR(4, 4) FSDP_RSAR(4, 2) FSDP_RSAR(4, 1) FSDP_RSAR(2, 2) FSDP_RSAR(2, 1)
 #undef FSDP_RSAR

@@ -70,6 +70,18 @@ def test_wide_meshes(S, D, dts):
     check_every_step(L, unit, alloc, seed=S * 100 + D, ops=("avg",))
 
 
+@pytest.mark.parametrize("W,S", [(16, 8), (8, 4), (8, 8), (8, 1), (16, 16), (16, 4), (4, 4), (4, 2),
+                                 (4, 1), (2, 2), (2, 1), (12, 3)])
+def test_every_compiled_mesh_shape(W, S):
+    # the bf16 fused reduce is compiled per mesh shape (the last case takes
+    # the generic kernel); shards longer than a 256-element step, some
+    # aligned with their sources and some shifted (odd-sized vectors move
+    # every later offset), so each shape's fast paths run, including the
+    # fan-out to several replicas
+    plan, L, unit, alloc = make(S, W // S, [1500, 7, 4099, 33], [17, 16, 1, 64], "bf16", "bf16")
+    check_every_step(L, unit, alloc, seed=W * 100 + S, ops=("avg", "sum"))
+
+
 @pytest.mark.parametrize("offsets", [
     # sources shifted against 16-byte boundaries, destinations aligned: funnel-shift path
     {"shards": 2, "grads": 6, "ag_output": 0},
