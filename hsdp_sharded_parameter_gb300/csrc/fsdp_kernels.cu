@@ -48,12 +48,16 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxStagedSources = 32;
 // The fused reduce fans a step's result out with TMA bulk stores (one
-// shared-memory image, one bulk store per destination) when it has at least
-// this many destinations (replicas); below, each lane stores its granule.
-constexpr int kFanOutDests = 4;
+// shared-memory image, one bulk store per destination) instead of having
+// each lane store its granule to every replica: with 4 or more replicas
+// (pure-TP layer, 8: 0.855 -> 0.903 of the measured copy peak), and with 2
+// when there are at most 8 sources (HSDP (2,4): 0.948 -> 0.961); the (2,8)
+// mesh's 16 sources measured slower with it (0.939 -> 0.924).
 constexpr size_t kFanImgBytes = kStepElems * sizeof(float);  // one step of fp32
-template <int KIND, int ND>
-__host__ __device__ constexpr bool fan_out() { return KIND == K_RSAR && ND >= kFanOutDests; }
+template <int KIND, int NS, int ND>
+__host__ __device__ constexpr bool fan_out() {
+    return KIND == K_RSAR && NS > 0 && (ND >= 4 || (ND >= 2 && NS <= 8));
+}
 // Resident blocks of the staged reduce its shared memory allows for 16 bf16
 // sources (69 KB each); telling the compiler so lets it keep the unrolled
 // fold in registers (up to 170 each) instead of spilling.
@@ -840,7 +844,7 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
         }
         Raw<float> o;
         narrow(total, o);
-        if (fan_out<KIND, ND>()) {
+        if constexpr (fan_out<KIND, NS, ND>()) {
             // the step's 256 results as one image (two per warp, in turn;
             // an image is rewritten only after the bulk stores of two fast
             // steps ago have read it), written to every replica by lane 0
@@ -858,10 +862,10 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
                 bulk_commit();
             }
             parity ^= 1;
-            return;
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
+            for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
+        }
         return;
     }
     if (rel >= st.n || rel + kGran <= 0) return;
@@ -927,7 +931,7 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
     extern __shared__ __align__(16) char smem_raw[];
     const Shape<KIND, NS, SIN, ND> sh(a);
     const size_t sb = Staging<S>::stage_bytes(sh.ns, sh.nd);
-    constexpr bool kFan = fan_out<KIND, ND>();
+    constexpr bool kFan = fan_out<KIND, NS, ND>();
     char* base = smem_raw + (threadIdx.x >> 5) * (2 * sb + (kFan ? 2 * kFanImgBytes : 0));
     char* here = base;        // stage of the step being folded
     char* there = base + sb;  // stage of the step in flight
@@ -1199,7 +1203,7 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
 #define FSDP_RSAR(W_, S_)                                                                               \
     if (a.W == W_ && a.S == S_)                                                                         \
         return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, W_ / S_, \
-                                   fan_out<K_RSAR, W_ / S_>());
+                                   fan_out<K_RSAR, W_, W_ / S_>());
             FSDP_RSAR(16, 8) FSDP_RSAR(8, 4) FSDP_RSAR(8, 8) FSDP_RSAR(8, 1) FSDP_RSAR(16, 16)
             FSDP_RSAR(16, 4) FSDP_RSAR(4, 4) FSDP_RSAR(4, 2) FSDP_RSAR(4, 1) FSDP_RSAR(2, 2) FSDP_RSAR(2, 1)
 #undef FSDP_RSAR
