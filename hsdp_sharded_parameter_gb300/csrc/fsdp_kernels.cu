@@ -540,7 +540,31 @@ __device__ __forceinline__ void apply_body(const KArgs& a) {
 #pragma unroll
                 for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
             } else {
-                load_tile_shifted(r, t0 - sh, (uintptr_t)(kStepElems * 4), sh, lane, kSteps);
+                // fp32 source off the 16-byte grid by whole elements: lane l
+                // takes elements l, l+32, ..., l+224 of every step, so each
+                // load reads 128 contiguous bytes of the warp and needs no
+                // realignment (far fewer registers than shuffling 16-byte
+                // blocks into place); the stores follow the same mapping
+                const float* s0 = src + cur.rel0 + lane;
+#pragma unroll
+                for (int u = 0; u < kSteps; ++u)
+#pragma unroll
+                    for (int i = 0; i < kGran; ++i) r[u].w[i] = __float_as_uint(__ldcs(s0 + u * kStepElems + i * 32));
+                if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
+                D* d0 = dst + cur.rel0 + lane;
+#pragma unroll
+                for (int u = 0; u < kSteps; ++u)
+#pragma unroll
+                    for (int i = 0; i < kGran; ++i) {
+                        const int64_t e = u * kStepElems + i * 32;
+                        float q = __uint_as_float(r[u].w[i]);
+                        if (scale) q = scaled(q, a);
+                        if (a.accumulate) q = __fadd_rn(load_f32(d0, e), q);
+                        store_f32(d0, e, q);
+                    }
+                cur = nxt;
+                t = tn;
+                continue;
             }
             if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
 #pragma unroll
