@@ -66,6 +66,7 @@ def lib():
         L.fsdp_plan_destroy.argtypes = [vp]
         L.fsdp_plan_upload.argtypes = [vp]
         L.fsdp_plan_set_grid_limit.argtypes = [vp, i32]
+        L.fsdp_plan_check_tables.argtypes = [vp]
         L.fsdp_plan_info.argtypes = [vp, P(i32), P(i32), P(i32), P(i32), P(i64)]
         L.fsdp_slice_numel.argtypes = [vp, i32, P(i64)]
         L.fsdp_sharded_size.argtypes = [vp, i32, i32, P(i64), P(i64)]
@@ -143,6 +144,12 @@ class Plan:
 
     def upload(self):
         _check(lib().fsdp_plan_upload(self.handle))
+        return self
+
+    def check_tables(self):
+        """Host-side bounds and coverage check of the plan's work tables
+        (no GPU needed); raises FsdpError naming the first violation."""
+        _check(lib().fsdp_plan_check_tables(self.handle))
         return self
 
     def set_grid_limit(self, max_blocks):

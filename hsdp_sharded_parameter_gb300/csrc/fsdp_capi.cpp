@@ -9,9 +9,11 @@
 //   [RAGGED]  FSDP dim-0 uneven-sharding RFC (hyper-parallel issue 319)
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstring>
 #include <new>
 #include <string>
+#include <utility>
 
 #include "fsdp_internal.h"
 
@@ -127,6 +129,73 @@ void build_tables(const fsdp_plan_s& pl, std::vector<Seg> segs[T_COUNT],
         if (sf > 0) segs[T_AR].push_back(make_seg(sf, 0, 0, 0, s));
     tile_prefix(segs[T_AR], 4, tiles[T_AR]);
 }
+
+namespace {
+
+// One table's runs against the buffers its kernel reads and writes:
+// dst_len(g) / src_len(g) give the element count of the buffer a run writes
+// / reads (-1: the run reads nothing); rows_of(g) the destination extent the
+// runs of that row must tile exactly (each element written once), keyed by
+// key(g). Returns "" or the first violation.
+template <typename DstLen, typename SrcLen, typename Key>
+std::string check_runs(const char* name, const std::vector<Seg>& segs, const std::vector<int64_t>& tiles,
+                       int dst_es, DstLen dst_len, SrcLen src_len, Key key,
+                       const std::vector<std::pair<int64_t, int64_t>>& extents) {
+    char buf[256];
+    if (tiles.size() != segs.size() + 1 || tiles[0] != 0) return std::string(name) + ": bad tile prefix size";
+    // destination coverage per key: sorted runs must tile [lo, hi) exactly
+    std::vector<std::vector<std::pair<int64_t, int64_t>>> cover(extents.size());
+    for (size_t k = 0; k < segs.size(); ++k) {
+        const Seg& g = segs[k];
+        const int64_t phase = ((g.dst_off * dst_es) & 15) / dst_es;
+        if (g.n <= 0) {
+            snprintf(buf, sizeof buf, "%s: run %zu is empty", name, k);
+            return buf;
+        }
+        if (tiles[k + 1] - tiles[k] != (g.n + phase + kWarpTile - 1) / kWarpTile) {
+            snprintf(buf, sizeof buf, "%s: run %zu has a wrong tile count", name, k);
+            return buf;
+        }
+        const int64_t dl = dst_len(g), sl = src_len(g);
+        if (g.dst_off < 0 || g.dst_off + g.n > dl) {
+            snprintf(buf, sizeof buf, "%s: run %zu writes [%lld, %lld) of a %lld-element buffer", name, k,
+                     (long long)g.dst_off, (long long)(g.dst_off + g.n), (long long)dl);
+            return buf;
+        }
+        if (sl >= 0 && (g.src_off < 0 || g.src_off + g.n > sl)) {
+            snprintf(buf, sizeof buf, "%s: run %zu reads [%lld, %lld) of a %lld-element buffer", name, k,
+                     (long long)g.src_off, (long long)(g.src_off + g.n), (long long)sl);
+            return buf;
+        }
+        const size_t c = key(g);
+        if (c >= cover.size()) {
+            snprintf(buf, sizeof buf, "%s: run %zu has an out-of-range key", name, k);
+            return buf;
+        }
+        cover[c].push_back({g.dst_off, g.dst_off + g.n});
+    }
+    for (size_t c = 0; c < cover.size(); ++c) {
+        auto& v = cover[c];
+        std::sort(v.begin(), v.end());
+        int64_t at = extents[c].first;
+        for (const auto& r : v) {
+            if (r.first != at) {
+                snprintf(buf, sizeof buf, "%s: destination %zu %s at element %lld", name, c,
+                         r.first > at ? "has a gap" : "is written twice", (long long)at);
+                return buf;
+            }
+            at = r.second;
+        }
+        if (at != extents[c].second) {
+            snprintf(buf, sizeof buf, "%s: destination %zu ends at %lld, not %lld", name, c, (long long)at,
+                     (long long)extents[c].second);
+            return buf;
+        }
+    }
+    return "";
+}
+
+}  // namespace
 
 }  // namespace fsdp
 
@@ -363,6 +432,75 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
     }
     pl->device = dev;
     pl->uploaded = true;
+    return FSDP_OK;
+}
+
+int fsdp_plan_check_tables(fsdp_plan_t pl) {
+    clear_error();
+    FSDP_CHECK_PLAN(pl);
+    std::vector<Seg> segs[T_COUNT];
+    std::vector<int64_t> tiles[T_COUNT];
+    build_tables(*pl, segs, tiles);
+    const int S = pl->S, P = pl->P;
+    auto shard_n = [&](int p, int s) { return pl->len[(size_t)p * S + s] * pl->inner[p]; };
+    auto full_n = [&](int p) { return pl->d0[p] * pl->inner[p]; };
+    const int64_t sf = pl->slice(FSDP_F32);
+    const std::vector<std::pair<int64_t, int64_t>> none;
+    std::string err;
+    // one extent per shard row s of a slice-sized region
+    auto rows = [&](int64_t sl, bool stacked) {
+        std::vector<std::pair<int64_t, int64_t>> v;
+        for (int s = 0; s < S; ++s) v.push_back({stacked ? s * sl : 0, stacked ? (s + 1) * sl : sl});
+        return v;
+    };
+    std::vector<std::pair<int64_t, int64_t>> per_param;
+    for (int p = 0; p < P; ++p) per_param.push_back({0, full_n(p)});
+    std::vector<std::pair<int64_t, int64_t>> per_shard;  // key p*S + s
+    for (int p = 0; p < P; ++p)
+        for (int s = 0; s < S; ++s) per_shard.push_back({0, shard_n(p, s)});
+    auto row_key = [](const Seg& g) { return (size_t)g.row; };
+    auto param_key = [](const Seg& g) { return (size_t)g.p; };
+
+    err = check_runs("fused RS+AR", segs[T_RSAR], tiles[T_RSAR], 4, [&](const Seg&) { return sf; },
+                     [&](const Seg& g) { return g.p < 0 ? (int64_t)-1 : full_n(g.p); }, row_key, rows(sf, false));
+    for (int i = 0; i < 2 && err.empty(); ++i) {
+        const int dt = i == 0 ? FSDP_F32 : FSDP_BF16, es = elem_size(dt);
+        const int64_t sl = pl->slice(dt);
+        const char* tag = i == 0 ? " (f32)" : " (bf16)";
+        err = check_runs((std::string("all-gather copy-in") + tag).c_str(), segs[T_AGIN_F32 + i], tiles[T_AGIN_F32 + i],
+                         es, [&](const Seg&) { return S * sl; },
+                         [&](const Seg& g) { return g.p < 0 ? (int64_t)-1 : shard_n(g.p, g.row); }, row_key,
+                         rows(sl, true));
+        if (err.empty())
+            err = check_runs((std::string("all-gather") + tag).c_str(), segs[T_GATHER_F32 + i],
+                             tiles[T_GATHER_F32 + i], es, [&](const Seg&) { return S * sl; },
+                             [&](const Seg&) { return S * sl; }, row_key, rows(sl, true));
+        if (err.empty())
+            err = check_runs((std::string("copy-out") + tag).c_str(), segs[T_AGOUT_F32 + i], tiles[T_AGOUT_F32 + i],
+                             es, [&](const Seg& g) { return full_n(g.p); }, [&](const Seg&) { return S * sl; },
+                             param_key, per_param);
+        if (err.empty())
+            err = check_runs((std::string("direct unshard") + tag).c_str(), segs[T_UNSHARD_F32 + i],
+                             tiles[T_UNSHARD_F32 + i], es, [&](const Seg& g) { return full_n(g.p); },
+                             [&](const Seg& g) { return shard_n(g.p, g.row); }, param_key, per_param);
+        if (err.empty())
+            err = check_runs((std::string("RS copy-in") + tag).c_str(), segs[T_RSIN_F32 + i], tiles[T_RSIN_F32 + i],
+                             es, [&](const Seg&) { return S * sl; },
+                             [&](const Seg& g) { return g.p < 0 ? (int64_t)-1 : full_n(g.p); }, row_key,
+                             rows(sl, true));
+        if (err.empty())
+            err = check_runs((std::string("unfused RS") + tag).c_str(), segs[T_RS_F32 + i], tiles[T_RS_F32 + i], 4,
+                             [&](const Seg&) { return sf; }, [&](const Seg&) { return S * sl; }, row_key,
+                             rows(sf, false));
+    }
+    if (err.empty())
+        err = check_runs("apply", segs[T_APPLY], tiles[T_APPLY], 4,
+                         [&](const Seg& g) { return shard_n(g.p, g.row); }, [&](const Seg&) { return sf; },
+                         [&](const Seg& g) { return (size_t)g.p * S + g.row; }, per_shard);
+    if (err.empty())
+        err = check_runs("unfused AR", segs[T_AR], tiles[T_AR], 4, [&](const Seg&) { return sf; },
+                         [&](const Seg&) { return sf; }, row_key, rows(sf, false));
+    if (!err.empty()) return set_error(FSDP_ERR_INVALID_ARG, "plan_check_tables: " + err);
     return FSDP_OK;
 }
 

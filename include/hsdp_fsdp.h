@@ -148,6 +148,16 @@ int fsdp_plan_upload(fsdp_plan_t plan);
  * between calls. */
 int fsdp_plan_set_grid_limit(fsdp_plan_t plan, int max_blocks);
 
+/* Diagnostic, with no counterpart in the pages: builds the plan's work
+ * tables on the host, as fsdp_plan_upload does, and checks every run
+ * against the buffers its kernel touches, at the sizes fsdp_bind requires:
+ * each run reads and writes inside those buffers, the runs of every
+ * destination (a slice row, a full parameter, an actual shard) cover it
+ * exactly once, and each run's tile count matches the prefix the kernels
+ * search. Needs no GPU and changes nothing. Returns FSDP_OK, or
+ * FSDP_ERR_INVALID_ARG with the first violation in fsdp_last_error(). */
+int fsdp_plan_check_tables(fsdp_plan_t plan);
+
 /* Mesh sizes and the unpadded total sum_p chunk_p * inner_p. Any output
  * pointer may be NULL. */
 int fsdp_plan_info(fsdp_plan_t plan, int* rank_size, int* shard_size, int* dp_size,

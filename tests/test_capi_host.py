@@ -107,3 +107,25 @@ def test_bucket_order_is_checked():
     with pytest.raises(C.FsdpError) as e:
         C.Plan([4, 4], [1, 1], 4, 4, bucket=[1, 0])
     assert e.value.code == C.FSDP_ERR_INVALID_ARG and "bucket" in str(e.value)
+
+
+# Host-side sanitizer of the work tables (compute-sanitizer is not used):
+# every run of every kernel's table reads and writes inside the buffers at
+# the sizes the bindings require, every destination is covered exactly once,
+# and the tile prefix the kernels search matches the runs.
+@pytest.mark.parametrize("key", WL.ORDER)
+def test_workload_tables_stay_in_bounds(key):
+    wl = WL.WORKLOADS[key]
+    C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).check_tables()
+
+
+def test_random_plan_tables_stay_in_bounds():
+    rng = np.random.default_rng(2024)
+    for _ in range(300):
+        P = int(rng.integers(1, 12))
+        S, D = int(rng.integers(1, 17)), int(rng.integers(1, 5))
+        d0 = [int(x) for x in rng.integers(0, 3000, P)]
+        d0[int(rng.integers(0, P))] = int(rng.integers(0, S + 1))  # short params: empty shards
+        inner = [int(x) for x in rng.choice([1, 2, 3, 7, 64, 127, 4096], P)]
+        bucket = sorted(int(x) for x in rng.integers(0, 4, P)) if rng.integers(0, 2) else None
+        C.Plan(d0, inner, S * D, S, bucket=bucket).check_tables()
