@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <map>
 #include <mutex>
 #include <unordered_map>
 
@@ -1096,30 +1097,36 @@ struct LaunchShape {
     int per_sm;
 };
 
+// SM count of the current device, cached per device (a process may launch
+// on several GPUs).
 int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0, v = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n = v > 0 ? v : 1;
-    }
-    return n;
+    static std::mutex mu;
+    static std::unordered_map<int, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return cache.emplace(dev, v > 0 ? v : 1).first->second;
 }
 
 // Resident blocks per SM for (kernel, block size, dynamic shared memory),
 // cached. Raises the kernel's dynamic shared memory limit when needed.
 int blocks_per_sm(const void* fn, int threads, size_t smem) {
     static std::mutex mu;
-    static std::unordered_map<const void*, std::unordered_map<size_t, int>> cache;
+    // keyed by (device, kernel): function attributes are set per device
+    static std::map<std::pair<int, const void*>, std::unordered_map<size_t, int>> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
-    auto fit = cache.find(fn);
+    auto fit = cache.find({dev, fn});
     if (fit == cache.end()) {
         // allow the device's whole opt-in shared memory (less the kernel's
-        // static shared memory) once per kernel, so any later launch of it
-        // (any table size) fits
-        int dev = 0, optin = 0;
-        cudaGetDevice(&dev);
+        // static shared memory) once per kernel and device, so any later
+        // launch of it (any table size) fits
+        int optin = 0;
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         cudaFuncAttributes fa;
         if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess) {
@@ -1129,7 +1136,7 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
         } else {
             (void)cudaGetLastError();
         }
-        fit = cache.emplace(fn, std::unordered_map<size_t, int>()).first;
+        fit = cache.emplace(std::make_pair(dev, fn), std::unordered_map<size_t, int>()).first;
     }
     auto& per = fit->second;
     auto it = per.find(smem);
