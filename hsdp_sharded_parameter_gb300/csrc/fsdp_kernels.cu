@@ -13,20 +13,27 @@
 //     the next tile's run is looked up while the current tile's loads are in
 //     flight.
 //   * Granules are anchored at 16-byte boundaries of the destination, so
-//     every full granule is written with aligned 16-byte stores. Partial
-//     granules (run heads/tails) and destinations that are not 16-byte
-//     aligned go element by element.
+//     every full granule is written with aligned 16-byte stores. A tile whose
+//     granules are all full (a whole tile, or the whole steps left of a short
+//     run) loads every step before storing; partial granules (run heads and
+//     tails) and destinations that are not 16-byte aligned go element by
+//     element.
 //   * Copy kernels read with aligned 16-byte loads into registers; a source
 //     run shifted against its destination (ragged offsets) is realigned with
 //     funnel shifts, each lane taking its neighbour block from the next lane
 //     by a warp shuffle. Kernels that write one tile to several destinations
 //     (fused copy-in, gather, direct unshard) stage it in shared memory once
 //     and fan it out with TMA bulk stores.
+//   * The apply kernel reads the fp32 fused region; a shifted source is off
+//     by whole elements, so it switches to a strided lane mapping (lane l
+//     takes elements l, l+32, ...) whose loads need no realignment.
 //   * Reduce kernels (W sources per output) stage each warp step's source
 //     windows in shared memory with cp.async (16-byte copies, one aligned
 //     window per source, one block wider when shifted) two steps deep, so
 //     the bytes in flight do not depend on registers, then fold from shared
-//     memory in the fixed order.
+//     memory in the fixed order. With several replicas to write, a step's
+//     result goes to shared memory once and out to every replica by TMA bulk
+//     stores (see fan_out).
 //   * Every staged or loaded 16-byte block holds at least one byte of its
 //     source run, so no access leaves the source allocation's pages.
 //
