@@ -14,7 +14,7 @@
  *             write-up under it ("方案落地说明")
  *   [RAGGED]  FSDP dim-0 uneven-sharding RFC (hyper-parallel issue 319)
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - rank w of the W = rank_size ranks sits at mesh coordinate
  *     (d, s) = (w / S, w % S): replicate index outer, shard rank inner;
  *   - the fused buffer holds the raw SUM over all W ranks; AVG divides once
