@@ -129,3 +129,11 @@ def test_random_plan_tables_stay_in_bounds():
         inner = [int(x) for x in rng.choice([1, 2, 3, 7, 64, 127, 4096], P)]
         bucket = sorted(int(x) for x in rng.integers(0, 4, P)) if rng.integers(0, 2) else None
         C.Plan(d0, inner, S * D, S, bucket=bucket).check_tables()
+
+
+def test_tables_of_a_very_long_parameter_list_stay_in_bounds():
+    rng = np.random.default_rng(5)
+    P = 100_000
+    d0 = [int(x) for x in rng.integers(0, 20, P)]
+    inner = [int(x) for x in rng.choice([1, 2, 5, 64], P)]
+    C.Plan(d0, inner, 16, 8).check_tables()

@@ -171,3 +171,14 @@ def test_bucketed_plans(seed):
     bucket = sorted(int(x) for x in rng.integers(0, 4, len(d0)))
     plan, L, unit, alloc = make(S, D, d0, inner, pdt, gdt, adt, bucket=bucket)
     check_every_step(L, unit, alloc, seed=seed)
+
+
+def test_many_small_parameters():
+    # thousands of tiny runs per table (the lookup's multi-round search,
+    # zero-length shards, one-row parameters), every output byte checked
+    rng = np.random.default_rng(77)
+    P = 1500
+    d0 = [int(x) for x in rng.integers(0, 10, P)]
+    inner = [int(x) for x in rng.choice([1, 3, 8], P)]
+    plan, L, unit, alloc = make(4, 1, d0, inner, "bf16", "bf16")
+    check_every_step(L, unit, alloc, seed=78, ops=("avg",))
