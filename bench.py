@@ -143,6 +143,28 @@ def algorithmic_bytes(sizes, param_dt, ag_dt, grad_dt):
     }
 
 
+def unfused_bytes(sizes, param_dt, ag_dt, grad_dt):
+    """Algorithmic bytes of the calls outside the timed step: the unfused
+    forward (copy-in of the own slice, then the all-gather) and the unfused
+    gradient sync (RS copy-in, shard-group ReduceScatter, replicate-group
+    AllReduce in place, apply). sizes as for algorithmic_bytes plus
+    slice_grad."""
+    W, S, N, D = sizes["W"], sizes["S"], sizes["N"], sizes["W"] // sizes["S"]
+    st = sizes["shard_total"]
+    bp, ba, bg = ES[param_dt], ES[ag_dt], ES[grad_dt]
+    sa, sg, sf = sizes["slice_ag"], sizes["slice_grad"], sizes["slice_f32"]
+    return {
+        "ag_copy_in_own_slice": st * bp + W * sa * ba,
+        # every rank's own slice read once, written to the S-1 other members
+        "ag_gather": (W * sa * ba + W * (S - 1) * sa * ba) if S > 1 else 0,
+        # full gradients read (padding not read), whole RS input rows written
+        "rs_copy_in": W * N * bg + W * S * sg * bg,
+        "rs_reduce": W * S * sg * bg + W * sf * 4,
+        "ar_reduce": 2 * W * sf * 4 if D > 1 else 0,
+        "apply_grads": st * 4 + st * bg,
+    }
+
+
 def plan_sizes(plan):
     W, S, P = plan.W, plan.S, plan.P
     N = sum(plan.numel(p) for p in range(P))
@@ -350,12 +372,13 @@ def run_gpu(args, wl):
     d0 = wl.d0 if args.scale == 1.0 else scaled_workload(wl, args.scale)[0]
     workload_name = wl.key if args.scale == 1.0 else f"{wl.key}@dim0x{args.scale:g}"
     plan = C.Plan(d0, wl.inner, wl.rank_size, wl.shard_size).upload()
-    unit = HsdpUnit(plan, wl.param_dtype, wl.grad_dtype, device=dev)
+    unit = HsdpUnit(plan, wl.param_dtype, wl.grad_dtype, device=dev, with_unfused=True)
     WL.torch_fill_(unit.shards, wl.seed_params, wl.param_std, wl.param_dtype)
     WL.torch_fill_(unit.grads, wl.seed_grads, wl.grad_std, wl.grad_dtype)
     sizes = plan_sizes(plan)
     sizes["slice_ag"] = plan.slice_numel(wl.param_dtype)
     sizes["slice_f32"] = plan.slice_numel("f32")
+    sizes["slice_grad"] = plan.slice_numel(wl.grad_dtype)
     kb = algorithmic_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype)
     step_bytes = sum(kb.values())
     working_set = step_bytes  # every byte of the step is a distinct HBM location
@@ -416,37 +439,59 @@ def run_gpu(args, wl):
     roofline_2 = {"bound": "hbm", "kernel": second, "achieved": kernels[second]["gbs"], "peak": peak,
                   "unit": "GB/s", "frac": kernels[second]["frac"], "traffic": ncu_traffic(second, workload_name)}
 
-    # Not part of the step: the direct unshard (all three forward steps in
-    # one pass, no gathered buffer), timed alone on the same unit. It reads
-    # each shard once and writes it into every shard-group member's full
-    # parameter.
-    extra = {}
-    ev_u = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for _ in range(2):
-        unit.unshard_direct()
-    torch.cuda.synchronize()
+    # Not part of the step, each call timed alone on the same unit: the
+    # direct unshard (all three forward steps in one pass, no gathered
+    # buffer: it reads each shard once and writes it into every shard-group
+    # member's full parameter), and the unfused calls (the own-slice copy-in
+    # and the all-gather of the forward; RS copy-in, ReduceScatter, in-place
+    # AllReduce and apply of the pages' unfused gradient sync).
     ku = max(3, K // 4)
-    if flush:  # time each launch alone, the L2 flush outside the events
-        ms_u = 0.0
-        for _ in range(ku):
-            scratch.zero_()
+
+    def per_launch_us(fn):
+        ev_u = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        if flush:  # time each launch alone, the L2 flush outside the events
+            ms_u = 0.0
+            for _ in range(ku):
+                scratch.zero_()
+                ev_u[0].record(stream)
+                fn()
+                ev_u[1].record(stream)
+                torch.cuda.synchronize()
+                ms_u += ev_u[0].elapsed_time(ev_u[1])
+        else:
             ev_u[0].record(stream)
-            unit.unshard_direct()
+            for _ in range(ku):
+                fn()
             ev_u[1].record(stream)
             torch.cuda.synchronize()
-            ms_u += ev_u[0].elapsed_time(ev_u[1])
-    else:
-        ev_u[0].record(stream)
-        for _ in range(ku):
-            unit.unshard_direct()
-        ev_u[1].record(stream)
-        torch.cuda.synchronize()
-        ms_u = ev_u[0].elapsed_time(ev_u[1])
-    us = ms_u / ku * 1e3
+            ms_u = ev_u[0].elapsed_time(ev_u[1])
+        return ms_u / ku * 1e3
+
+    def entry(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
+        return {"us": round(us, 2), "bytes": nbytes, "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    extra = {}
     ub = sizes["shard_total"] * ES[wl.param_dtype] + sizes["W"] * sizes["N"] * ES[wl.param_dtype]
-    extra["ag_unshard"] = {"us": round(us, 2), "bytes": ub, "gbs": round(ub / (us * 1e-6) / 1e9, 1),
-                           "frac": round(ub / (us * 1e-6) / 1e9 / peak, 4),
-                           "replaces_us": round(kernels["ag_copy_in"]["us"] + kernels["ag_copy_out"]["us"], 2)}
+    extra["ag_unshard"] = entry(per_launch_us(unit.unshard_direct), ub)
+    extra["ag_unshard"]["replaces_us"] = round(kernels["ag_copy_in"]["us"] + kernels["ag_copy_out"]["us"], 2)
+    ubytes = unfused_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype)
+    unfused_calls = {
+        "ag_copy_in_own_slice": lambda: unit.ag_copy_in(fuse_gather=False),
+        "ag_gather": unit.ag_gather,
+        "rs_copy_in": lambda: C.fsdp_rs_copy_in(plan, unit.b_grads, unit.b_rs_in),
+        "rs_reduce": lambda: C.fsdp_rs_reduce(plan, unit.b_rs_in, "avg", unit.b_fused),
+        "ar_reduce": lambda: C.fsdp_ar_reduce(plan, unit.b_fused, "avg"),
+    }
+    unfused = {n: entry(per_launch_us(fn), ubytes[n]) for n, fn in unfused_calls.items()}
+    sync_us = sum(unfused[n]["us"] for n in ["rs_copy_in", "rs_reduce", "ar_reduce"]) + kernels["apply_grads"]["us"]
+    unfused["sync_total"] = {"us": round(sync_us, 2),
+                             "replaces_us": round(kernels["rs_ar_reduce"]["us"] + kernels["apply_grads"]["us"], 2),
+                             "note": "RS copy-in + ReduceScatter + AllReduce + apply (SUM after the collectives' AVG)"}
+    extra["unfused"] = unfused
 
     if args.graph:
         graph = unit.capture_step()

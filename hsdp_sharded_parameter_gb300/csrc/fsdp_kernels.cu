@@ -318,6 +318,8 @@ __device__ __forceinline__ int64_t warp_count() { return ((int64_t)gridDim.x * b
 // K_GATHER: ag[(d,s)] slice s -> ag[(d,s')] slice s, s' != s. rep = d.
 // K_AGOUT : ag[w] at s*slice + o_p -> full[w,p] rows [off, off+len). rep = w.
 // K_RSIN  : grads[w,p] rows [off, off+len) -> rs_in[w] row s. rep = w.
+// K_RS    : (shard groups of one rank only) rs_in[(d,0)] row 0 -> fused[(d,0)],
+//           widened to fp32: the ReduceScatter of one term. rep = d.
 template <int KIND, typename S>
 __device__ __forceinline__ const S* copy_src(const KArgs& a, const Tile& ti) {
     if (KIND == K_AGIN)
@@ -327,6 +329,7 @@ __device__ __forceinline__ const S* copy_src(const KArgs& a, const Tile& ti) {
     if (KIND == K_AGOUT) return static_cast<const S*>(a.src_tab[ti.rep]);
     if (KIND == K_UNSHARD)
         return static_cast<const S*>(a.src_tab[(int64_t)(ti.rep * a.S + ti.row) * a.P + ti.p]);
+    if (KIND == K_RS) return static_cast<const S*>(a.src_tab[ti.rep * a.S + ti.row]);
     return ti.p >= 0 ? static_cast<const S*>(a.src_tab[(int64_t)ti.rep * a.P + ti.p]) : nullptr;
 }
 
@@ -349,6 +352,8 @@ __device__ __forceinline__ D* copy_dst(const KArgs& a, const Tile& ti, int j) {
         d = static_cast<D*>(a.dst_tab[(int64_t)ti.rep * a.P + ti.p]);
     else if (KIND == K_UNSHARD)  // shard-group member j of replica rep
         d = static_cast<D*>(a.dst_tab[(int64_t)(ti.rep * a.S + j) * a.P + ti.p]);
+    else if (KIND == K_RS)
+        d = static_cast<D*>(a.dst_tab[ti.rep * a.S + ti.row]);
     else
         d = static_cast<D*>(a.dst_tab[ti.rep]);
     return d + ti.dst_off;
@@ -1072,6 +1077,10 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
 template <typename S, typename D>
 __global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
+// The unfused ReduceScatter over a shard group of one rank: a widening copy
+// (the sum of one term, divided by 1).
+template <typename S>
+__global__ void __launch_bounds__(kThreads) rs_reduce_copy_kernel(const KArgs a) { copy_body<K_RS, S, float, false>(a); }
 template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
@@ -1204,11 +1213,19 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     return cudaGetLastError();
 }
 
+// Blocks per SM of the unfused ReduceScatter: with few sources a step moves
+// few bytes, so it needs more warps than the fused reduce's policy gives
+// (HSDP (2,4), 4 sources: 0.758 -> 0.992 of the measured copy peak at 4
+// blocks per SM); with 8 or more the fused reduce's policy measured best.
+int rs_grid(int ns) { return ns <= 4 ? 4 : -1; }
+// per_sm < 0: the plan's staged_blocks (the fused reduce's policy); 0: as
+// many blocks as fit; > 0: that many.
 template <typename S, typename F>
-cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan = false) {
+cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan = false,
+                      int per_sm = -1) {
     const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * kFanImgBytes : 0);
-    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp,
-              FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks);
+    const int grid = per_sm >= 0 ? per_sm : (FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks);
+    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, grid);
 }
 
 // The staged reduce fits when its per-block shared memory stays well inside
@@ -1258,13 +1275,18 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
 #undef FSDP_RSAR
             return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, 0, 0, 0>, a, st, a.W, a.D);
         case K_RS:
+            // one rank per shard group: a widening copy
+            if (a.S == 1)
+                return sf ? go(rs_reduce_copy_kernel<float>, a, st)
+                          : go(rs_reduce_copy_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
             if (sf)
-                return staged_fits<float>(a.S, 1) ? go_staged<float>(rs_reduce_kernel<float, 0>, a, st, a.S, 1)
-                                                  : go(rs_reduce_wide_kernel<float>, a, st);
+                return staged_fits<float>(a.S, 1)
+                           ? go_staged<float>(rs_reduce_kernel<float, 0>, a, st, a.S, 1, false, rs_grid(a.S))
+                           : go(rs_reduce_wide_kernel<float>, a, st);
             if (!staged_fits<uint16_t>(a.S, 1)) return go(rs_reduce_wide_kernel<uint16_t>, a, st);
-            if (a.S == 8) return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 8>, a, st, 8, 1);
-            if (a.S == 4) return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 4>, a, st, 4, 1);
-            return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 0>, a, st, a.S, 1);
+            if (a.S == 8) return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 8>, a, st, 8, 1, false, rs_grid(8));
+            if (a.S == 4) return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 4>, a, st, 4, 1, false, rs_grid(4));
+            return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 0>, a, st, a.S, 1, false, rs_grid(a.S));
         case K_AR:
             if (!staged_fits<float>(a.D, a.D)) return go(ar_reduce_wide_kernel, a, st);
             if (a.D == 2) return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2);

@@ -27,6 +27,25 @@ def test_algorithmic_bytes_of_the_large_layer():
     assert b["apply_grads"] == 2 * N * 6 == 10_267_852_800
 
 
+def test_unfused_bytes_of_the_large_layer():
+    # the same layer; every slice is N/S elements (no tail), D = 2 replicas
+    N, W, S = 855_654_400, 16, 8
+    sl = N // S
+    sizes = {"W": W, "S": S, "N": N, "shard_total": 2 * N, "slice_ag": sl, "slice_f32": sl,
+             "slice_grad": sl}
+    b = bench.unfused_bytes(sizes, "bf16", "bf16", "bf16")
+    assert b["ag_copy_in_own_slice"] == 2 * N * 2 + W * sl * 2 == 6_845_235_200
+    assert b["ag_gather"] == W * sl * 2 * S == 27_380_940_800   # read once, written to 7 others
+    assert b["rs_copy_in"] == W * N * 2 * 2 == 54_761_881_600
+    assert b["rs_reduce"] == W * S * sl * 2 + W * sl * 4 == 34_226_176_000
+    assert b["ar_reduce"] == 2 * W * sl * 4 == 13_690_470_400
+    # one rank per shard group: no gather; one replica: no all-reduce
+    one = dict(sizes, S=1, slice_ag=N, slice_f32=N, slice_grad=N, shard_total=W * N)
+    assert bench.unfused_bytes(one, "bf16", "bf16", "bf16")["ag_gather"] == 0
+    full = dict(sizes, W=S)
+    assert bench.unfused_bytes(full, "bf16", "bf16", "bf16")["ar_reduce"] == 0
+
+
 def test_reference_arm_prints_the_contract_line():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--workload", "tiny_fsdp", "--steps", "2", "--warmup", "1"],
