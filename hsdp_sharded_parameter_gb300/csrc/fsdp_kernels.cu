@@ -62,9 +62,12 @@ constexpr int kMaxStagedSources = 32;
 // when there are at most 8 sources (HSDP (2,4): 0.948 -> 0.961); the (2,8)
 // mesh's 16 sources measured slower with it (0.939 -> 0.924).
 constexpr size_t kFanImgBytes = kStepElems * sizeof(float);  // one step of fp32
+// The unfused AllReduce fans out from 4 replicas on (pure-TP, 8: 0.84 ->
+// 0.90; with 2 it measured slower, 0.878 -> 0.841).
 template <int KIND, int NS, int ND>
 __host__ __device__ constexpr bool fan_out() {
-    return KIND == K_RSAR && NS > 0 && (ND >= 4 || (ND >= 2 && NS <= 8));
+    return (KIND == K_RSAR && NS > 0 && (ND >= 4 || (ND >= 2 && NS <= 8))) ||
+           (KIND == K_AR && NS > 0 && ND >= 4);
 }
 // Resident blocks of the staged reduce its shared memory allows for 16 bf16
 // sources (69 KB each); telling the compiler so lets it keep the unrolled
@@ -1170,8 +1173,9 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 // several waves; each warp still strides over the whole table):
 //   copy-out 16 (0.955 -> 1.006 of the measured copy peak), fused copy-in
 //   32 (0.889 -> 0.998), apply 16 (0.967 -> 0.992), direct unshard 32
-//   (0.90 -> 0.999). The staged reduce takes KArgs::staged_blocks, which
-//   the plan derives from its layout (0 here = use that hint).
+//   (0.90 -> 0.999), the unfused all-gather 32 (0.89 -> 0.98). The staged
+//   reduce takes KArgs::staged_blocks, which the plan derives from its
+//   layout (0 here = use that hint).
 #ifndef FSDP_GRID_COPY
 #define FSDP_GRID_COPY 16
 #endif
@@ -1186,6 +1190,9 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #endif
 #ifndef FSDP_GRID_UNSHARD
 #define FSDP_GRID_UNSHARD 32
+#endif
+#ifndef FSDP_GRID_GATHER
+#define FSDP_GRID_GATHER 32
 #endif
 
 template <typename F>
@@ -1248,7 +1255,7 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
                       FSDP_GRID_MULTI);
         case K_GATHER:
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
-                      : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+                      : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(), FSDP_GRID_GATHER);
         case K_UNSHARD:
             if (sf && df) return go(ag_unshard_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
             if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
@@ -1289,8 +1296,8 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 0>, a, st, a.S, 1, false, rs_grid(a.S));
         case K_AR:
             if (!staged_fits<float>(a.D, a.D)) return go(ar_reduce_wide_kernel, a, st);
-            if (a.D == 2) return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2);
-            if (a.D == 8) return go_staged<float>(ar_reduce_kernel<8>, a, st, 8, 8);
+            if (a.D == 2) return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2, fan_out<K_AR, 2, 2>());
+            if (a.D == 8) return go_staged<float>(ar_reduce_kernel<8>, a, st, 8, 8, fan_out<K_AR, 8, 8>());
             return go_staged<float>(ar_reduce_kernel<0>, a, st, a.D, a.D);
         case K_APPLY:
             return df ? go(apply_grads_kernel<float>, a, st)
