@@ -1167,32 +1167,43 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 }
 
 // Blocks per SM of each kernel family's grid: 0 = as many as fit at once
-// (one persistent wave). DRAM throughput depends on how many warps stream
-// at the same time, not monotonically, so each family has its own value,
-// chosen by a sweep on the large HSDP layer (a value above what fits gives
-// several waves; each warp still strides over the whole table):
-//   copy-out 16 (0.955 -> 1.006 of the measured copy peak), fused copy-in
-//   32 (0.889 -> 0.998), apply 16 (0.967 -> 0.992), direct unshard 32
-//   (0.90 -> 0.999), the unfused all-gather 32 (0.89 -> 0.98). The staged
-//   reduce takes KArgs::staged_blocks, which the plan derives from its
-//   layout (0 here = use that hint).
+// (one persistent wave). A value above what fits gives many waves of
+// short-lived blocks; each warp still strides over the whole table, but it
+// handles few tiles, so the tiles in flight at any time form one
+// contiguous window of the table, and that measured faster than a
+// persistent grid. Each family has the value its sweep chose (large (2,8)
+// layer unless noted; fraction of the measured copy peak):
+//   copy-out 128 (one wave 0.955, 16: 1.006, 128: 1.019; 256 was no better
+//     there and slower on the ragged layer, 0.967 -> 0.955),
+//   fused copy-in 256 (one wave 0.889, 32: 0.981, 256: 0.998),
+//   direct unshard 256 (one wave 0.90, 32: 0.983, 256: 0.999),
+//   apply 64 (16: 0.998, 64: 1.02; ragged 0.884 -> 0.913),
+//   unfused all-gather 256 (one wave 0.89, 32: 0.98, 256: 1.01-1.03).
+// The fused reduce's value is in rsar_grid(); the unfused reduces take
+// KArgs::staged_blocks, which the plan derives from its layout, or
+// rs_grid().
 #ifndef FSDP_GRID_COPY
-#define FSDP_GRID_COPY 16
+#define FSDP_GRID_COPY 128
 #endif
 #ifndef FSDP_GRID_MULTI
-#define FSDP_GRID_MULTI 32
+#define FSDP_GRID_MULTI 256
 #endif
 #ifndef FSDP_GRID_APPLY
-#define FSDP_GRID_APPLY 16
+#define FSDP_GRID_APPLY 64
 #endif
 #ifndef FSDP_GRID_STAGED
 #define FSDP_GRID_STAGED 0
 #endif
 #ifndef FSDP_GRID_UNSHARD
-#define FSDP_GRID_UNSHARD 32
+#define FSDP_GRID_UNSHARD 256
 #endif
 #ifndef FSDP_GRID_GATHER
-#define FSDP_GRID_GATHER 32
+#define FSDP_GRID_GATHER 256
+#endif
+// The unfused copy-in of the own slice only (one destination): 32 (large
+// 0.999, ragged 0.80; at 256 the ragged layer measured 0.71).
+#ifndef FSDP_GRID_OWN
+#define FSDP_GRID_OWN 32
 #endif
 
 template <typename F>
@@ -1220,11 +1231,28 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     return cudaGetLastError();
 }
 
-// Blocks per SM of the unfused ReduceScatter: with few sources a step moves
-// few bytes, so it needs more warps than the fused reduce's policy gives
-// (HSDP (2,4), 4 sources: 0.758 -> 0.992 of the measured copy peak at 4
-// blocks per SM); with 8 or more the fused reduce's policy measured best.
-int rs_grid(int ns) { return ns <= 4 ? 4 : -1; }
+// Blocks per SM of the fused reduce. Without fan-out it runs many waves of
+// short-lived blocks (the tiles in flight at any time then form one
+// contiguous window of the table): large (2,8) layer 0.948 -> 1.046 of the
+// measured copy peak, ragged 0.918 -> 1.001 at 256 blocks per SM (64:
+// 1.025 / 0.988, 128: 1.037 / 0.998). Shapes
+// that fan out to their replicas measured slower that way (HSDP (2,4)
+// 0.960 -> 0.939, pure-TP 0.922 -> 0.887; each block drains its bulk stores
+// before it exits) and keep the plan's staged_blocks (one wave).
+#ifndef FSDP_GRID_RSAR
+#define FSDP_GRID_RSAR 256
+#endif
+int rsar_grid(bool fan) { return fan ? -1 : FSDP_GRID_RSAR; }
+
+// Blocks per SM of the unfused ReduceScatter: with 4 sources or fewer a
+// step moves few bytes and one wave of 4 blocks per SM measured best (HSDP
+// (2,4): 0.758 -> 0.992 of the measured copy peak; many waves 0.935); with
+// 8 or more, many waves like the fused reduce (large 0.94 -> 1.02, ragged
+// 0.93 -> 1.03).
+int rs_grid(int ns) { return ns <= 4 ? 4 : FSDP_GRID_RSAR; }
+// The unfused AllReduce without fan-out also runs many waves (large layer,
+// 2 replicas: 0.886 -> 1.012); with fan-out it keeps one wave.
+int ar_grid(bool fan) { return fan ? -1 : FSDP_GRID_RSAR; }
 // per_sm < 0: the plan's staged_blocks (the fused reduce's policy); 0: as
 // many blocks as fit; > 0: that many.
 template <typename S, typename F>
@@ -1252,7 +1280,7 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             if (sf && df) return go(ag_copy_in_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
             if (sf) return go(ag_copy_in_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
             return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
-                      FSDP_GRID_MULTI);
+                      a.fuse ? FSDP_GRID_MULTI : FSDP_GRID_OWN);
         case K_GATHER:
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
                       : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(), FSDP_GRID_GATHER);
@@ -1269,18 +1297,20 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
         case K_RSAR:
             if (sf) {
                 if (!staged_fits<float>(a.W, a.D)) return go(rs_ar_reduce_wide_kernel<float>, a, st);
-                if (a.W == 4 && a.S == 4) return go_staged<float>(rs_ar_reduce_kernel<float, 4, 4, 1>, a, st, 4, 1);
-                return go_staged<float>(rs_ar_reduce_kernel<float, 0, 0, 0>, a, st, a.W, a.D);
+                if (a.W == 4 && a.S == 4)
+                    return go_staged<float>(rs_ar_reduce_kernel<float, 4, 4, 1>, a, st, 4, 1, false, rsar_grid(false));
+                return go_staged<float>(rs_ar_reduce_kernel<float, 0, 0, 0>, a, st, a.W, a.D, false, rsar_grid(false));
             }
             if (!staged_fits<uint16_t>(a.W, a.D)) return go(rs_ar_reduce_wide_kernel<uint16_t>, a, st);
 #define FSDP_RSAR(W_, S_)                                                                               \
     if (a.W == W_ && a.S == S_)                                                                         \
         return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, W_ / S_, \
-                                   fan_out<K_RSAR, W_, W_ / S_>());
+                                   fan_out<K_RSAR, W_, W_ / S_>(), rsar_grid(fan_out<K_RSAR, W_, W_ / S_>()));
             FSDP_RSAR(16, 8) FSDP_RSAR(8, 4) FSDP_RSAR(8, 8) FSDP_RSAR(8, 1) FSDP_RSAR(16, 16)
             FSDP_RSAR(16, 4) FSDP_RSAR(4, 4) FSDP_RSAR(4, 2) FSDP_RSAR(4, 1) FSDP_RSAR(2, 2) FSDP_RSAR(2, 1)
 #undef FSDP_RSAR
-            return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, 0, 0, 0>, a, st, a.W, a.D);
+            return go_staged<uint16_t>(rs_ar_reduce_kernel<uint16_t, 0, 0, 0>, a, st, a.W, a.D, false,
+                                       rsar_grid(false));
         case K_RS:
             // one rank per shard group: a widening copy
             if (a.S == 1)
@@ -1296,9 +1326,13 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 0>, a, st, a.S, 1, false, rs_grid(a.S));
         case K_AR:
             if (!staged_fits<float>(a.D, a.D)) return go(ar_reduce_wide_kernel, a, st);
-            if (a.D == 2) return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2, fan_out<K_AR, 2, 2>());
-            if (a.D == 8) return go_staged<float>(ar_reduce_kernel<8>, a, st, 8, 8, fan_out<K_AR, 8, 8>());
-            return go_staged<float>(ar_reduce_kernel<0>, a, st, a.D, a.D);
+            if (a.D == 2)
+                return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2, fan_out<K_AR, 2, 2>(),
+                                        ar_grid(fan_out<K_AR, 2, 2>()));
+            if (a.D == 8)
+                return go_staged<float>(ar_reduce_kernel<8>, a, st, 8, 8, fan_out<K_AR, 8, 8>(),
+                                        ar_grid(fan_out<K_AR, 8, 8>()));
+            return go_staged<float>(ar_reduce_kernel<0>, a, st, a.D, a.D, false, ar_grid(false));
         case K_APPLY:
             return df ? go(apply_grads_kernel<float>, a, st)
                       : go(apply_grads_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_APPLY);
