@@ -1205,6 +1205,11 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #ifndef FSDP_GRID_OWN
 #define FSDP_GRID_OWN 32
 #endif
+// The unfused RS copy-in (large 0.956 -> 1.013, HSDP (2,4) 0.952 -> 1.015
+// at 128 against one wave).
+#ifndef FSDP_GRID_RSIN
+#define FSDP_GRID_RSIN 128
+#endif
 
 template <typename F>
 cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0,
@@ -1293,7 +1298,8 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return sf ? go(ag_copy_out_kernel<float>, a, st)
                       : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
         case K_RSIN:
-            return sf ? go(rs_copy_in_kernel<float>, a, st) : go(rs_copy_in_kernel<uint16_t>, a, st);
+            return sf ? go(rs_copy_in_kernel<float>, a, st)
+                      : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);
         case K_RSAR:
             if (sf) {
                 if (!staged_fits<float>(a.W, a.D)) return go(rs_ar_reduce_wide_kernel<float>, a, st);
