@@ -1133,6 +1133,9 @@ int sm_count() {
 
 // Resident blocks per SM for (kernel, block size, dynamic shared memory),
 // cached. Raises the kernel's dynamic shared memory limit when needed.
+// See go(): run count above which a short launch keeps one wave.
+constexpr int kWaveMaxRuns = 256;
+
 int blocks_per_sm(const void* fn, int threads, size_t smem) {
     static std::mutex mu;
     // keyed by (device, kernel): function attributes are set per device
@@ -1219,14 +1222,17 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     const int resident = blocks_per_sm(fn, threads, smem);  // also raises the smem limit once
     const int64_t warps = a.ntiles * a.reps;
     int per_sm = grid_per_sm > 0 ? grid_per_sm : resident;
-    // Several waves pay off only for long launches; a launch with fewer than
-    // 100 tiles per resident warp (many small runs) stays at one wave (the
-    // pure-TP layer, ~80 tiles per warp, measured slower with several:
-    // copy-in 0.886 -> 0.865, copy-out 0.934 -> 0.909, apply 0.940 -> 0.872
-    // of the measured copy peak). A tile written to several destinations
-    // counts once per destination.
+    // Many waves pay off unless a launch is short AND its table is long: a
+    // warp's first lookup searches the runs from the start, and with few
+    // tiles per warp that search is paid over and over. A launch with fewer
+    // than 100 tiles per resident warp over more than kWaveMaxRuns runs
+    // (the 2000-parameter pure-TP layer: copy-in 0.884 at one wave, 0.759
+    // with many) stays at one wave; a short launch over few runs takes many
+    // (HSDP (2,4) apply, 36 runs: 0.967 -> 1.000). A tile written to several
+    // destinations counts once per destination.
     const int64_t dests = a.fuse ? a.S : (a.dests > 1 ? a.dests : 1);
-    if (per_sm > resident && warps * dests < (int64_t)resident * sm_count() * (threads / 32) * 100)
+    if (per_sm > resident && a.nseg > kWaveMaxRuns &&
+        warps * dests < (int64_t)resident * sm_count() * (threads / 32) * 100)
         per_sm = resident;
     const int64_t want = (warps + threads / 32 - 1) / (threads / 32);
     int64_t cap = (int64_t)sm_count() * per_sm;
