@@ -63,6 +63,7 @@ enum TableId {
 struct Table {
     const Seg* segs = nullptr;           // device
     const int64_t* tile_begin = nullptr; // device, nseg + 1
+    const int32_t* tile_run = nullptr;   // device, ntiles: the run of each tile
     int nseg = 0;
     int64_t ntiles = 0;
 };
@@ -73,6 +74,9 @@ inline int elem_size(int dt) { return dt == FSDP_F32 ? 4 : (dt == FSDP_BF16 ? 2 
 struct KArgs {
     const Seg* segs;
     const int64_t* tile_begin;
+    // The run of every tile (ntiles entries), or nullptr: a lookup that
+    // jumps past the next run reads it here instead of searching the prefix.
+    const int32_t* tile_run;
     int nseg;
     int64_t ntiles;  // tiles of one repetition
     int reps;        // repetitions of the table (ranks or replicas)

@@ -270,11 +270,14 @@ __device__ __forceinline__ void copy_elem(D* dst, int64_t di, const S* src, int6
 // Largest k with tb[k] <= tile, searching forward from k (tb strictly
 // increasing, tb[k] <= tile < tb[nseg]). Warp-uniform; all 32 lanes take
 // part. The common case (same or next run) costs one or two loads; a longer
-// jump narrows [lo, hi) 32-fold per round: lane i probes lo + i*step and a
-// ballot counts the probes at or below the tile (they form a prefix).
-__device__ __forceinline__ int find_seg(const int64_t* __restrict__ tb, int nseg, int k, int64_t tile) {
+// jump reads the plan's tile -> run map (one load) or, without one, narrows
+// [lo, hi) 32-fold per round: lane i probes lo + i*step and a ballot counts
+// the probes at or below the tile (they form a prefix).
+__device__ __forceinline__ int find_seg(const int64_t* __restrict__ tb, const int32_t* __restrict__ run, int nseg,
+                                        int k, int64_t tile) {
     if (tile < __ldg(tb + k + 1)) return k;
     if (k + 2 > nseg || tile < __ldg(tb + k + 2)) return k + 1;
+    if (run) return __ldg(run + tile);  // a longer jump: the plan's tile -> run map
     const int lane = threadIdx.x & 31;
     int lo = k + 1, hi = nseg;  // tb[lo] <= tile < tb[hi]
     while (hi - lo > 1) {
@@ -301,7 +304,7 @@ struct Tile {
 __device__ __forceinline__ void lookup(const KArgs& a, int64_t t, int& k, int dst_es, Tile& ti) {
     const int64_t tile = t / a.reps;
     ti.rep = (int)(t - tile * a.reps);
-    k = find_seg(a.tile_begin, a.nseg, k, tile);
+    k = find_seg(a.tile_begin, a.tile_run, a.nseg, k, tile);
     const Seg sg = a.segs[k];
     ti.n = sg.n;
     ti.dst_off = sg.dst_off;
@@ -1135,6 +1138,7 @@ int sm_count() {
 // cached. Raises the kernel's dynamic shared memory limit when needed.
 // See go(): run count above which a short launch keeps one wave.
 constexpr int kWaveMaxRuns = 256;
+
 
 int blocks_per_sm(const void* fn, int threads, size_t smem) {
     static std::mutex mu;
