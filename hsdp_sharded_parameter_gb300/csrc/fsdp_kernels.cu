@@ -373,7 +373,15 @@ __device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t b
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// Waits until every bulk store of this thread has read its shared-memory
+// source (the wait before a block exits and its shared memory is reused);
+// their global writes complete on their own, and the kernel's end orders
+// them before later work on the stream. Waiting for the writes too at every
+// block's exit measured slower once grids run many short waves (HSDP (2,4)
+// fused reduce 0.959 -> 1.032 with this wait and many waves).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
 // Orders this thread's shared-memory writes before later async-proxy
 // (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -504,8 +512,8 @@ __device__ __forceinline__ void copy_body(const KArgs& a) {
         cur = nxt;
         t = tn;
     }
-    // bulk stores still reading shared memory or writing must finish
-    if (MULTI && lane == 0) bulk_wait_all();
+    // bulk stores must have read the tile images before the block exits
+    if (MULTI && lane == 0) bulk_wait_read_all();
 }
 
 // ------------------------------------------------------------ apply kernel
@@ -997,8 +1005,8 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
         there = t;
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-    // bulk stores still reading the images or writing must finish
-    if (kFan && (threadIdx.x & 31) == 0) bulk_wait_all();
+    // bulk stores must have read the images before the block exits
+    if (kFan && (threadIdx.x & 31) == 0) bulk_wait_read_all();
 }
 
 // Register path for more than kMaxStagedSources sources: each lane loads
@@ -1218,9 +1226,11 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #define FSDP_GRID_RSIN 128
 #endif
 
+// fallback_per_sm: blocks per SM when the launch stays at one wave (0 = as
+// many as fit).
 template <typename F>
 cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0,
-               int grid_per_sm = 0) {
+               int grid_per_sm = 0, int fallback_per_sm = 0) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     sm_count();
     const int resident = blocks_per_sm(fn, threads, smem);  // also raises the smem limit once
@@ -1237,7 +1247,7 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     const int64_t dests = a.fuse ? a.S : (a.dests > 1 ? a.dests : 1);
     if (per_sm > resident && a.nseg > kWaveMaxRuns &&
         warps * dests < (int64_t)resident * sm_count() * (threads / 32) * 100)
-        per_sm = resident;
+        per_sm = fallback_per_sm > 0 && fallback_per_sm < resident ? fallback_per_sm : resident;
     const int64_t want = (warps + threads / 32 - 1) / (threads / 32);
     int64_t cap = (int64_t)sm_count() * per_sm;
     if (a.max_grid > 0 && a.max_grid < cap) cap = a.max_grid;
@@ -1246,18 +1256,17 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     return cudaGetLastError();
 }
 
-// Blocks per SM of the fused reduce. Without fan-out it runs many waves of
-// short-lived blocks (the tiles in flight at any time then form one
-// contiguous window of the table): large (2,8) layer 0.948 -> 1.046 of the
-// measured copy peak, ragged 0.918 -> 1.001 at 256 blocks per SM (64:
-// 1.025 / 0.988, 128: 1.037 / 0.998). Shapes
-// that fan out to their replicas measured slower that way (HSDP (2,4)
-// 0.960 -> 0.939, pure-TP 0.922 -> 0.887; each block drains its bulk stores
-// before it exits) and keep the plan's staged_blocks (one wave).
+// Blocks per SM of the fused reduce: many waves of short-lived blocks (the
+// tiles in flight at any time then form one contiguous window of the
+// table): large (2,8) layer 0.948 -> 1.046 of the measured copy peak,
+// ragged 0.918 -> 1.001 at 256 blocks per SM (64: 1.025 / 0.988, 128:
+// 1.037 / 0.998); with the read-only exit wait the shapes that fan out to
+// their replicas gain too (HSDP (2,4) 0.959 -> 1.032). A launch that stays
+// at one wave (the 2000-parameter layer) uses the plan's staged_blocks.
 #ifndef FSDP_GRID_RSAR
 #define FSDP_GRID_RSAR 256
 #endif
-int rsar_grid(bool fan) { return fan ? -1 : FSDP_GRID_RSAR; }
+int rsar_grid(bool) { return FSDP_GRID_RSAR; }
 
 // Blocks per SM of the unfused ReduceScatter: with 4 sources or fewer a
 // step moves few bytes and one wave of 4 blocks per SM measured best (HSDP
@@ -1274,8 +1283,8 @@ template <typename S, typename F>
 cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan = false,
                       int per_sm = -1) {
     const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * kFanImgBytes : 0);
-    const int grid = per_sm >= 0 ? per_sm : (FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks);
-    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, grid);
+    const int policy = FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks;
+    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, per_sm >= 0 ? per_sm : policy, policy);
 }
 
 // The staged reduce fits when its per-block shared memory stays well inside
