@@ -135,12 +135,15 @@ int fsdp_plan_create_bucketed(int n_params, const int64_t* dim0, const int64_t* 
 int fsdp_plan_destroy(fsdp_plan_t plan);
 
 /* Uploads the plan's work tables to the current CUDA device (synchronous,
- * allocates device memory once). Required before any data call; data calls
- * must then run with that device current. Calling it again is a no-op. */
+ * allocates device memory once: 40 bytes per run of each kernel's table,
+ * plus, for tables of more than 1024 runs, 4 bytes per 2048 elements the
+ * table covers). Required before any data call; data calls must then run
+ * with that device current. Calling it again is a no-op. */
 int fsdp_plan_upload(fsdp_plan_t plan);
 
 /* Caps the number of thread blocks every later data call of this plan
- * launches (0, the default: one persistent wave over the whole GPU). The
+ * launches (0, the default: each kernel's own grid, many short waves of
+ * blocks on long launches). The
  * kernels stride over their work, so any cap gives the same results; a
  * small cap leaves the other SMs to kernels running beside them, e.g. the
  * backward compute the gradient sync overlaps with, the way the pages'
