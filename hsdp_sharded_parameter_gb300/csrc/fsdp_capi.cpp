@@ -402,6 +402,13 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
             if ((((g.src_off - (g.dst_off & 3)) * 2) & 15) != 0) shifted += g.n;
         }
         pl->staged_blocks = 2 * shifted > total ? 3 : 2;
+        // the same measure for the bf16 copy-out (16-byte aligned buffers)
+        shifted = total = 0;
+        for (const Seg& g : segs[T_AGOUT_BF16]) {
+            total += g.n;
+            if ((((g.src_off - g.dst_off) * 2) & 15) != 0) shifted += g.n;
+        }
+        pl->agout_shifted = 2 * shifted > total;
     }
     // Per table: the runs, the tile prefix and, for tables of more than
     // kMapMinRuns runs, the run of every tile, so that a lookup that jumps
@@ -710,6 +717,7 @@ int fsdp_ag_copy_out(fsdp_plan_t pl, fsdp_binding_t ag_out, fsdp_binding_t full,
     a.src_tab = ag_out->dev_table;
     a.dst_tab = full->dev_table;
     a.vec = full->aligned16;
+    a.shifted = pl->agout_shifted ? 1 : 0;
     return run(K_AGOUT, ag_out->dt, full->dt, a, stream, "ag_copy_out");
 }
 

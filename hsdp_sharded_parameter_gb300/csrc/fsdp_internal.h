@@ -100,6 +100,9 @@ struct KArgs {
     // 3 when most runs are shifted (their steps do more work per byte, so
     // more warps are needed to keep the same bytes in flight).
     int staged_blocks;
+    // Most of the table's data sits in runs whose source is shifted against
+    // the destination's 16-byte grid (copy-out picks its grid by it).
+    int shifted;
     int dests;  // destinations written per tile when more than one (the gather)
 };
 
@@ -136,6 +139,7 @@ struct fsdp_plan_s {
     bool uploaded = false;
     int max_grid = 0;  // fsdp_plan_set_grid_limit
     int staged_blocks = 2;  // see KArgs::staged_blocks, set by fsdp_plan_upload
+    bool agout_shifted = false;  // see KArgs::shifted (bf16 copy-out), set by fsdp_plan_upload
     void* dev_block = nullptr;
     fsdp::Table tables[fsdp::T_COUNT];
     int64_t slice(int dt) const {

@@ -1189,7 +1189,8 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 // persistent grid. Each family has the value its sweep chose (large (2,8)
 // layer unless noted; fraction of the measured copy peak):
 //   copy-out 128 (one wave 0.955, 16: 1.006, 128: 1.019; 256 was no better
-//     there and slower on the ragged layer, 0.967 -> 0.955),
+//     there), 16 when most of the plan's copy-out data is shifted
+//     (FSDP_GRID_COPY_SHIFTED),
 //   fused copy-in 256 (one wave 0.889, 32: 0.981, 256: 0.998),
 //   direct unshard 256 (one wave 0.90, 32: 0.983, 256: 0.999),
 //   apply 64 (16: 0.998, 64: 1.02; ragged 0.884 -> 0.913),
@@ -1199,6 +1200,11 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 // rs_grid().
 #ifndef FSDP_GRID_COPY
 #define FSDP_GRID_COPY 128
+#endif
+// Copy-out of a plan whose data sits mostly in shifted runs (the ragged
+// layer: 0.960 at 128, 0.980 at 16; 32 and 64 in between).
+#ifndef FSDP_GRID_COPY_SHIFTED
+#define FSDP_GRID_COPY_SHIFTED 16
 #endif
 #ifndef FSDP_GRID_MULTI
 #define FSDP_GRID_MULTI 256
@@ -1315,7 +1321,8 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
                       FSDP_GRID_UNSHARD);
         case K_AGOUT:
             return sf ? go(ag_copy_out_kernel<float>, a, st)
-                      : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
+                      : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0,
+                           a.shifted ? FSDP_GRID_COPY_SHIFTED : FSDP_GRID_COPY);
         case K_RSIN:
             return sf ? go(rs_copy_in_kernel<float>, a, st)
                       : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);
