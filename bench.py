@@ -603,6 +603,9 @@ def run_pipeline(args, wl, d0, dev):
             t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap).run(compute))
             hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
             res[f"comm_blocks_{cap}"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
+        t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, sync_priority=0).run(compute))
+        hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
+        res["sync_low_priority"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
         out[name] = res
     for u in units:
         u.close()

@@ -154,18 +154,19 @@ class BackwardPipeline:
     fused kernel on the shard stream and are applied at the end. No call
     blocks the host; finish() waits on the host with a time limit."""
 
-    def __init__(self, units, op="avg", fused=False, comm_blocks=0):
+    def __init__(self, units, op="avg", fused=False, comm_blocks=0, sync_priority=-1):
         """comm_blocks > 0 caps the thread blocks of every sync kernel the
         pipeline issues (fsdp_plan_set_grid_limit), leaving the other SMs to
-        the backward compute; the sync streams get high priority so their
-        blocks are placed as soon as SMs free up."""
+        the backward compute. sync_priority is the sync streams' priority:
+        -1 (high, the default) places their blocks as soon as SMs free up;
+        0 (the compute stream's) lets compute blocks go first."""
         self.units = list(units)
         self.op = op
         self.fused = fused
         self.comm_blocks = comm_blocks
         dev = self.units[0].device if self.units else torch.device("cuda")
-        self.rs_stream = torch.cuda.Stream(device=dev, priority=-1)
-        self.ar_stream = torch.cuda.Stream(device=dev, priority=-1)
+        self.rs_stream = torch.cuda.Stream(device=dev, priority=sync_priority)
+        self.ar_stream = torch.cuda.Stream(device=dev, priority=sync_priority)
         self.log = []  # (step, layer) in issue order
 
     def _apply(self, L, stream=None):
