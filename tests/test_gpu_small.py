@@ -182,3 +182,27 @@ def test_many_small_parameters():
     inner = [int(x) for x in rng.choice([1, 3, 8], P)]
     plan, L, unit, alloc = make(4, 1, d0, inner, "bf16", "bf16")
     check_every_step(L, unit, alloc, seed=78, ops=("avg",))
+
+
+@pytest.mark.parametrize("cap", [1, 3, 7])
+@pytest.mark.parametrize("case", ["ragged", "fanout", "many_runs"])
+def test_grid_limits_give_the_same_bytes(case, cap):
+    # a grid capped to a few blocks (fsdp_plan_set_grid_limit) makes every
+    # warp stride over many tiles: long forward run lookups (search and
+    # tile map), the staged reduce's ring and the fan-out images over many
+    # steps; every output must still equal the oracle byte for byte
+    rng = np.random.default_rng(cap)
+    if case == "ragged":
+        S, D = 4, 2
+        d0 = [int(x) for x in rng.integers(1, 900, 6)] + [3, 1]
+        inner = [int(x) for x in rng.choice([1, 3, 64, 129], len(d0))]
+    elif case == "fanout":  # (8,1): 8 replicas, fan-out of the fused reduce and the AllReduce
+        S, D = 1, 8
+        d0, inner = [700, 5, 333], [17, 64, 1]
+    else:  # more than 1024 runs per table: the tile -> run map
+        S, D = 2, 2
+        d0 = [int(x) for x in rng.integers(0, 6, 700)]
+        inner = [int(x) for x in rng.choice([1, 8, 40], 700)]
+    plan, L, unit, alloc = make(S, D, d0, inner, "bf16", "bf16")
+    plan.set_grid_limit(cap)
+    check_every_step(L, unit, alloc, seed=10 * cap + len(case), ops=("avg",))
