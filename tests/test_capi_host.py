@@ -137,3 +137,43 @@ def test_tables_of_a_very_long_parameter_list_stay_in_bounds():
     d0 = [int(x) for x in rng.integers(0, 20, P)]
     inner = [int(x) for x in rng.choice([1, 2, 5, 64], P)]
     C.Plan(d0, inner, 16, 8).check_tables()
+
+
+def test_error_messages_are_per_thread():
+    # fsdp_last_error() is thread-local: threads that fail differently at the
+    # same time each read back their own message, while other threads build
+    # and check plans concurrently
+    import threading
+
+    lib = C.lib()
+    results, errors = {}, []
+    barrier = threading.Barrier(8)
+
+    def failing(i):
+        barrier.wait()
+        for _ in range(200):
+            d0 = (ctypes.c_int64 * 1)(7)
+            inner = (ctypes.c_int64 * 1)(8)
+            h = ctypes.c_void_p()
+            if i % 2:
+                rc = lib.fsdp_plan_create(1, d0, inner, 6, 4, 1, 0, ctypes.byref(h))  # 6 % 4 != 0
+            else:
+                rc = lib.fsdp_plan_create(1, d0, inner, 4, 4, 1, 1, ctypes.byref(h))  # shard_dim 1
+            msg = lib.fsdp_last_error().decode()
+            if (i % 2 and (rc != C.FSDP_ERR_INVALID_ARG or "shard_dim" in msg)) or \
+               (not i % 2 and (rc != C.FSDP_ERR_NOT_IMPLEMENTED or "shard_dim" not in msg)):
+                errors.append((i, rc, msg))
+        results[i] = True
+
+    def building(i):
+        barrier.wait()
+        for k in range(50):
+            C.Plan([7 + k, 16, 5], [8, 1, 3], 8, 4).check_tables()
+        results[i] = True
+
+    threads = [threading.Thread(target=failing if i < 6 else building, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert errors == [] and len(results) == 8
