@@ -94,7 +94,7 @@ struct KArgs {
     // agree bit for bit, subnormals included); 2 = IEEE division.
     int scale_mode;
     float recip;
-    int max_grid;  // upper bound on the launch's blocks (0 = one persistent wave)
+    int max_grid;  // upper bound on the launch's blocks (0 = the kernel's own grid)
     // Blocks per SM for the staged reduce (0 = as many as fit): 2 when most
     // of the fused region's data sits in runs aligned with their sources,
     // 3 when most runs are shifted (their steps do more work per byte, so
