@@ -1280,9 +1280,9 @@ int rsar_grid(bool) { return FSDP_GRID_RSAR; }
 // 8 or more, many waves like the fused reduce (large 0.94 -> 1.02, ragged
 // 0.93 -> 1.03).
 int rs_grid(int ns) { return ns <= 4 ? 4 : FSDP_GRID_RSAR; }
-// The unfused AllReduce without fan-out also runs many waves (large layer,
-// 2 replicas: 0.886 -> 1.012); with fan-out it keeps one wave.
-int ar_grid(bool fan) { return fan ? -1 : FSDP_GRID_RSAR; }
+// The unfused AllReduce also runs many waves (large layer, 2 replicas:
+// 0.886 -> 1.012; pure-TP, 8 replicas with fan-out: 0.90 -> 0.99).
+int ar_grid(bool) { return FSDP_GRID_RSAR; }
 // per_sm < 0: the plan's staged_blocks (the fused reduce's policy); 0: as
 // many blocks as fit; > 0: that many.
 template <typename S, typename F>
