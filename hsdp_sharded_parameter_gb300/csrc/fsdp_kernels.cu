@@ -1148,6 +1148,7 @@ int sm_count() {
 constexpr int kWaveMaxRuns = 256;
 
 
+
 int blocks_per_sm(const void* fn, int threads, size_t smem) {
     static std::mutex mu;
     // keyed by (device, kernel): function attributes are set per device
@@ -1233,10 +1234,11 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #endif
 
 // fallback_per_sm: blocks per SM when the launch stays at one wave (0 = as
-// many as fit).
+// many as fit). map_waves: a table with a tile -> run map is exempt from
+// the one-wave rule below.
 template <typename F>
 cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0,
-               int grid_per_sm = 0, int fallback_per_sm = 0) {
+               int grid_per_sm = 0, int fallback_per_sm = 0, bool map_waves = false) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     sm_count();
     const int resident = blocks_per_sm(fn, threads, smem);  // also raises the smem limit once
@@ -1251,7 +1253,7 @@ cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads
     // (HSDP (2,4) apply, 36 runs: 0.967 -> 1.000). A tile written to several
     // destinations counts once per destination.
     const int64_t dests = a.fuse ? a.S : (a.dests > 1 ? a.dests : 1);
-    if (per_sm > resident && a.nseg > kWaveMaxRuns &&
+    if (per_sm > resident && !(map_waves && a.tile_run) && a.nseg > kWaveMaxRuns &&
         warps * dests < (int64_t)resident * sm_count() * (threads / 32) * 100)
         per_sm = fallback_per_sm > 0 && fallback_per_sm < resident ? fallback_per_sm : resident;
     const int64_t want = (warps + threads / 32 - 1) / (threads / 32);
@@ -1290,7 +1292,10 @@ cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd,
                       int per_sm = -1) {
     const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * kFanImgBytes : 0);
     const int policy = FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks;
-    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, per_sm >= 0 ? per_sm : policy, policy);
+    // a staged reduce over a table with a tile -> run map takes many waves
+    // even when short (2000-parameter layer: fused reduce 0.927 -> 0.996)
+    return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, per_sm >= 0 ? per_sm : policy, policy,
+              true);
 }
 
 // The staged reduce fits when its per-block shared memory stays well inside
