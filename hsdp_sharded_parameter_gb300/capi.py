@@ -28,6 +28,8 @@ ROLES = {"shards": FSDP_ROLE_SHARDS, "ag_output": FSDP_ROLE_AG_OUTPUT,
          "rs_input": FSDP_ROLE_RS_INPUT, "fused": FSDP_ROLE_FUSED,
          "shard_grads": FSDP_ROLE_SHARD_GRADS}
 DTYPES = {"f32": FSDP_F32, "bf16": FSDP_BF16}
+# roles that take one buffer per (rank, parameter); the others one per rank
+PER_PARAM_ROLES = {FSDP_ROLE_SHARDS, FSDP_ROLE_FULL_PARAMS, FSDP_ROLE_GRADS, FSDP_ROLE_SHARD_GRADS}
 OPS = {"avg": FSDP_AVG, "sum": FSDP_SUM}
 
 _lib = None
@@ -203,11 +205,42 @@ class Plan:
         return Binding(self, role, dt, tensors, check_sizes)
 
 
+def _torch_dtype(dt):
+    import torch
+
+    return {FSDP_F32: torch.float32, FSDP_BF16: torch.bfloat16}.get(DTYPES.get(dt, dt))
+
+
+def _check_tensors(what, tensors, count, dt, numel_of=None):
+    """Host-side checks before a pointer array goes to the library, which
+    reads exactly `count` entries: the count, then (when dt is given) each
+    tensor's dtype, device and contiguity, and (numel_of(i)) its size."""
+    if len(tensors) != count:
+        raise FsdpError(FSDP_ERR_INVALID_ARG, f"{what}: {len(tensors)} tensors given, the plan needs {count}")
+    if dt is None:
+        return
+    want = _torch_dtype(dt)
+    for i, t in enumerate(tensors):
+        if t.dtype != want or not t.is_cuda or not t.is_contiguous():
+            raise FsdpError(FSDP_ERR_INVALID_ARG,
+                            f"{what}: tensor {i} is {t.dtype} on {t.device}"
+                            f"{'' if t.is_contiguous() else ', not contiguous'}; expected contiguous {want} on a GPU")
+        if numel_of is not None and t.numel() < numel_of(i):
+            raise FsdpError(FSDP_ERR_INVALID_ARG,
+                            f"{what}: tensor {i} holds {t.numel()} elements, needs {numel_of(i)}")
+
+
 class Binding:
     """Owns an fsdp_binding_t: a device table of the tensors' pointers.
-    Keeps the tensors alive while the binding lives."""
+    Keeps the tensors alive while the binding lives. The number of tensors
+    is always checked (the library reads W*P or W pointers); with
+    check_sizes (the default) their dtypes and sizes are checked too, the
+    sizes again by the library."""
 
     def __init__(self, plan, role, dt, tensors, check_sizes=True):
+        r = ROLES.get(role, role)
+        _check_tensors(f"bind {role}", tensors, plan.W * plan.P if r in PER_PARAM_ROLES else plan.W,
+                       dt if check_sizes else None)
         n = len(tensors)
         ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in tensors])
         numels = (ctypes.c_int64 * max(n, 1))(*[t.numel() for t in tensors])
@@ -273,7 +306,12 @@ def fsdp_rs_ar_reduce_noalloc(plan, grad_dt, grads, fused, stream=None):
     """The fused gradient sync without any device allocation by the library
     (for callers that cannot allocate device memory): ``plan`` needs no
     upload, ``grads`` (W*P tensors) and ``fused`` (W fp32 tensors) are passed
-    as pointer arrays on every call."""
+    as pointer arrays on every call. The library cannot see the tensors'
+    sizes here, so their count, dtype and size are checked before the call."""
+    P = plan.P
+    _check_tensors("rs_ar_reduce_noalloc grads", grads, plan.W * P, grad_dt, lambda i: plan.numel(i % P))
+    sf = plan.slice_numel("f32")
+    _check_tensors("rs_ar_reduce_noalloc fused", fused, plan.W, "f32", lambda i: sf)
     g = (ctypes.c_void_p * max(len(grads), 1))(*[t.data_ptr() for t in grads])
     f = (ctypes.c_void_p * max(len(fused), 1))(*[t.data_ptr() for t in fused])
     _check(lib().fsdp_rs_ar_reduce_noalloc(plan.handle, DTYPES.get(grad_dt, grad_dt), g, f,

@@ -43,25 +43,13 @@ Seg make_seg(int64_t n, int64_t dst_off, int64_t src_off, int p, int row) {
     return g;
 }
 
-// Runs of one slice row s: for every parameter with a non-empty shard s,
-// its actual elements at o_p, and zero runs for the padding rows between
-// them and for the tail up to row_len ([RAGGED §6.4]: padding is zero).
-// Adjacent zero runs are merged. data_src_full: the data run reads the full
-// tensor at off_{p,s} * inner (gradients); otherwise the shard from 0.
-void row_runs(const fsdp_plan_s& pl, int s, int64_t row_base, int64_t row_len,
-              bool data_src_full, std::vector<Seg>& out) {
-    int64_t zero_from = 0;
-    for (int p = 0; p < pl.P; ++p) {
-        int64_t n = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
-        if (n == 0) continue;
-        if (pl.o[p] > zero_from)
-            out.push_back(make_seg(pl.o[p] - zero_from, row_base + zero_from, 0, -1, s));
-        int64_t src = data_src_full ? pl.off[(size_t)p * pl.S + s] * pl.inner[p] : 0;
-        out.push_back(make_seg(n, row_base + pl.o[p], src, p, s));
-        zero_from = pl.o[p] + n;
-    }
-    if (row_len > zero_from)
-        out.push_back(make_seg(row_len - zero_from, row_base + zero_from, 0, -1, s));
+// The runs of one slice row (for_each_row_run) appended to out.
+void row_runs(const fsdp_plan_s& pl, int s, int64_t row_base, int64_t row_len, bool data_src_full,
+              std::vector<Seg>& out) {
+    for_each_row_run(pl, s, row_base, row_len, data_src_full,
+                     [&](int64_t n, int64_t dst_off, int64_t src_off, int p, int row) {
+                         out.push_back(make_seg(n, dst_off, src_off, p, row));
+                     });
 }
 
 void tile_prefix(const std::vector<Seg>& segs, int dst_es, std::vector<int64_t>& tiles) {
@@ -395,15 +383,9 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
     // against the fp32 destination's 16-byte grid (16-byte aligned buffers
     // assumed): picks the staged reduce's blocks per SM.
     {
-        int64_t shifted = 0, total = 0;
-        for (const Seg& g : segs[T_RSAR]) {
-            if (g.p < 0) continue;
-            total += g.n;
-            if ((((g.src_off - (g.dst_off & 3)) * 2) & 15) != 0) shifted += g.n;
-        }
-        pl->staged_blocks = 2 * shifted > total ? 3 : 2;
+        pl->staged_blocks = staged_blocks_for(segs[T_RSAR].data(), segs[T_RSAR].size());
         // the same measure for the bf16 copy-out (16-byte aligned buffers)
-        shifted = total = 0;
+        int64_t shifted = 0, total = 0;
         for (const Seg& g : segs[T_AGOUT_BF16]) {
             total += g.n;
             if ((((g.src_off - g.dst_off) * 2) & 15) != 0) shifted += g.n;

@@ -158,6 +158,44 @@ struct fsdp_binding_s {
 };
 
 namespace fsdp {
+
+// Runs of one slice row s: for every parameter with a non-empty shard s, its
+// actual elements at o_p, and zero runs for the padding rows between them
+// and for the tail up to row_len ([RAGGED §6.4]: padding is zero); adjacent
+// zero runs come out merged. data_src_full: a data run reads the full tensor
+// at off_{p,s} * inner (gradients); otherwise the shard from 0. Calls
+// emit(n, dst_off, src_off, p, row) once per run, in order, and allocates
+// nothing (the allocation-free entry point builds its table with it too).
+template <typename Emit>
+void for_each_row_run(const fsdp_plan_s& pl, int s, int64_t row_base, int64_t row_len, bool data_src_full,
+                      Emit&& emit) {
+    int64_t zero_from = 0;
+    for (int p = 0; p < pl.P; ++p) {
+        const int64_t n = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
+        if (n == 0) continue;
+        if (pl.o[p] > zero_from) emit(pl.o[p] - zero_from, row_base + zero_from, (int64_t)0, -1, s);
+        const int64_t src = data_src_full ? pl.off[(size_t)p * pl.S + s] * pl.inner[p] : 0;
+        emit(n, row_base + pl.o[p], src, p, s);
+        zero_from = pl.o[p] + n;
+    }
+    if (row_len > zero_from) emit(row_len - zero_from, row_base + zero_from, (int64_t)0, -1, s);
+}
+
+// Blocks per SM of the staged fused reduce for its run table (see
+// KArgs::staged_blocks): 3 when most of the data sits in runs whose bf16
+// source is shifted against the fp32 destination's 16-byte grid (16-byte
+// aligned buffers assumed), else 2.
+inline int staged_blocks_for(const Seg* segs, size_t nseg) {
+    int64_t shifted = 0, total = 0;
+    for (size_t k = 0; k < nseg; ++k) {
+        const Seg& g = segs[k];
+        if (g.p < 0) continue;
+        total += g.n;
+        if ((((g.src_off - (g.dst_off & 3)) * 2) & 15) != 0) shifted += g.n;
+    }
+    return 2 * shifted > total ? 3 : 2;
+}
+
 int set_error(int code, const std::string& msg);
 void clear_error();
 void count_launch();

@@ -53,34 +53,24 @@ int scratch_address(int dev, void** out) {
     return FSDP_OK;
 }
 
-// The runs of the fused region, shard row by shard row: each parameter's
-// actual elements at o_p and zero runs for padding rows and the slice tail
-// (the same runs, in the same order, as the uploaded table of the regular
-// fused sync). Writes up to `cap` runs; returns how many there are.
+// The runs of the fused region, shard row by shard row: the same builder,
+// in the same order, as the uploaded table of the regular fused sync
+// (fsdp::for_each_row_run). Writes up to `cap` runs; returns how many there
+// are.
 int64_t fused_runs(const fsdp_plan_s& pl, fsdp::Seg* out, int64_t cap) {
     const int64_t sf = pl.slice(FSDP_F32);
     int64_t n = 0;
-    auto emit = [&](int64_t cnt, int64_t dst_off, int64_t src_off, int p, int s) {
-        if (n < cap) {
-            out[n].n = cnt;
-            out[n].dst_off = dst_off;
-            out[n].src_off = src_off;
-            out[n].p = p;
-            out[n].row = s;
-        }
-        ++n;
-    };
-    for (int s = 0; s < pl.S; ++s) {
-        int64_t zero_from = 0;
-        for (int p = 0; p < pl.P; ++p) {
-            const int64_t cnt = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
-            if (cnt == 0) continue;
-            if (pl.o[p] > zero_from) emit(pl.o[p] - zero_from, zero_from, 0, -1, s);
-            emit(cnt, pl.o[p], pl.off[(size_t)p * pl.S + s] * pl.inner[p], p, s);
-            zero_from = pl.o[p] + cnt;
-        }
-        if (sf > zero_from) emit(sf - zero_from, zero_from, 0, -1, s);
-    }
+    for (int s = 0; s < pl.S; ++s)
+        fsdp::for_each_row_run(pl, s, 0, sf, true, [&](int64_t cnt, int64_t dst_off, int64_t src_off, int p, int row) {
+            if (n < cap) {
+                out[n].n = cnt;
+                out[n].dst_off = dst_off;
+                out[n].src_off = src_off;
+                out[n].p = p;
+                out[n].row = row;
+            }
+            ++n;
+        });
     return n;
 }
 
@@ -113,6 +103,17 @@ extern "C" int fsdp_rs_ar_reduce_noalloc(fsdp_plan_t pl, int grad_dtype, const v
         if (a & 15u) vec = false;
     }
 
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // The tables are staged through host memory that the next call reuses,
+    // so a copy recorded into a graph would replay another call's tables.
+    cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cap_status);
+    if (e != cudaSuccess) return set_error(FSDP_ERR_CUDA, std::string("rs_ar_reduce_noalloc: ") + cudaGetErrorString(e));
+    if (cap_status != cudaStreamCaptureStatusNone)
+        return set_error(FSDP_ERR_INVALID_ARG,
+                         "rs_ar_reduce_noalloc: the stream is being captured; this call stages its tables through "
+                         "a host buffer that later calls overwrite, so it is refused during capture");
+
     std::lock_guard<std::mutex> lock(g_mu);
     // layout: runs | tile prefix | gradient pointers [W][P] | fused pointers [W]
     Seg* runs = reinterpret_cast<Seg*>(g_host_stage);
@@ -138,11 +139,10 @@ extern "C" int fsdp_rs_ar_reduce_noalloc(fsdp_plan_t pl, int grad_dtype, const v
     std::memcpy(g_host_stage + off_dst, fused, (size_t)W * sizeof(void*));
 
     int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_error(FSDP_ERR_CUDA, std::string("rs_ar_reduce_noalloc: ") + cudaGetErrorString(e));
     void* scratch = nullptr;
     if (int rc = scratch_address(dev, &scratch)) return rc;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // Pageable source: the call returns once the bytes are staged, so the
     // host buffer may be reused right after; the copy is ordered before the
     // kernel on the same stream.
@@ -164,6 +164,10 @@ extern "C" int fsdp_rs_ar_reduce_noalloc(fsdp_plan_t pl, int grad_dtype, const v
     a.src_tab = reinterpret_cast<void* const*>(base + off_src);
     a.dst_tab = reinterpret_cast<void* const*>(base + off_dst);
     a.vec = vec ? 1 : 0;
+    // the plan's grid cap (fsdp_plan_set_grid_limit) and the staged reduce's
+    // blocks per SM, derived from the runs as fsdp_plan_upload derives them
+    a.max_grid = pl->max_grid;
+    a.staged_blocks = staged_blocks_for(runs, (size_t)nseg);
     set_divisor(a, 1);
     e = launch(K_RSAR, grad_dtype, FSDP_F32, a, st);
     if (e != cudaSuccess) return set_error(FSDP_ERR_CUDA, std::string("rs_ar_reduce_noalloc: ") + cudaGetErrorString(e));

@@ -320,8 +320,13 @@ int fsdp_ar_reduce(fsdp_plan_t plan, fsdp_binding_t fused, int op, fsdp_stream_t
  * into the array on `stream` ahead of the kernel and rewrites everything it
  * reads, so nothing in the array needs to start at zero; the array is
  * shared by all calls, so calls that overlap on the GPU (different streams,
- * no ordering between them) race on it and must not be issued. Host calls
- * are serialised by a lock. Returns as fsdp_rs_ar_reduce does. */
+ * no ordering between them) race on it and must not be issued. The tables
+ * are staged through one host buffer that the next call overwrites, so a
+ * call while `stream` is being captured is refused (FSDP_ERR_INVALID_ARG).
+ * A grid cap set with fsdp_plan_set_grid_limit applies here too. Host calls
+ * are serialised by a lock. The caller sizes both pointer arrays (W*P and
+ * W entries) and the buffers they point to; the library cannot check a
+ * buffer's size here. Returns as fsdp_rs_ar_reduce does. */
 int fsdp_rs_ar_reduce_noalloc(fsdp_plan_t plan, int grad_dtype, const void* const* grads,
                               float* const* fused, fsdp_stream_t stream);
 
