@@ -65,7 +65,6 @@ def lib():
         L.hor_ar_reduce.argtypes = [vp, i32, i64, vp]
         L.hor_apply_grads.argtypes = [vp, vp, i32, i32, i32, vp]
         L.hor_locate_fused_many.argtypes = [vp, i64, vp, vp, vp, vp]
-        L.hor_locate_slice_many.argtypes = [vp, i64, vp, vp, vp, vp]
         L.hor_locate_gathered_many.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp]
         L.hor_fold_nested_many.argtypes = [i32, i32, i64, vp, vp]
         L.hor_f32_to_bf16_many.argtypes = [i64, vp, vp]
@@ -245,15 +244,6 @@ def locate_fused(L, s, j):
     e = np.zeros(len(s), np.int64)
     lib().hor_locate_fused_many(L.c, len(s), _ptr(s), _ptr(j), _ptr(p), _ptr(e))
     return p, e
-
-
-def locate_slice(L, s, j):
-    s = np.ascontiguousarray(s, np.int32)
-    j = np.ascontiguousarray(j, np.int64)
-    p = np.zeros(len(s), np.int32)
-    k = np.zeros(len(s), np.int64)
-    lib().hor_locate_slice_many(L.c, len(s), _ptr(s), _ptr(j), _ptr(p), _ptr(k))
-    return p, k
 
 
 def locate_gathered(L, dt, p, e):

@@ -448,33 +448,6 @@ int hor_locate_fused(const hor_layout* L, int s, int64_t j, int64_t* e)
     return -1;
 }
 
-int hor_locate_slice(const hor_layout* L, int s, int64_t j, int64_t* k)
-{
-    /* Which shard element the all-gather copy-in puts at position j of
-     * shard s's slice: the parameter whose padded region holds j, element
-     * j - o_p of its shard when that lies inside the actual rows. Returns
-     * the parameter index, or -1 when j is padding. */
-    for (int p = 0; p < L->P; ++p) {
-        if (j >= L->o[p] && j < L->o[p] + L->dss[p] * L->inner[p]) {
-            int64_t rel = j - L->o[p];
-            if (rel >= L->len[(int64_t)p * L->S + s] * L->inner[p])
-                return -1;
-            *k = rel;
-            return p;
-        }
-    }
-    return -1;
-}
-
-void hor_locate_slice_many(const hor_layout* L, int64_t n, const int* s, const int64_t* j,
-                           int* p, int64_t* k)
-{
-    for (int64_t i = 0; i < n; ++i) {
-        k[i] = -1;
-        p[i] = hor_locate_slice(L, s[i], j[i], &k[i]);
-    }
-}
-
 int64_t hor_locate_gathered(const hor_layout* L, int64_t slice, int p, int64_t e,
                             int* shard, int64_t* k)
 {

@@ -54,9 +54,6 @@ int hor_apply_grads(const hor_layout* L, const float* const* fused, int op, int 
                     int accumulate, void* const* shard_grads);
 
 int hor_locate_fused(const hor_layout* L, int s, int64_t j, int64_t* e);
-int hor_locate_slice(const hor_layout* L, int s, int64_t j, int64_t* k);
-void hor_locate_slice_many(const hor_layout* L, int64_t n, const int* s, const int64_t* j,
-                           int* p, int64_t* k);
 int64_t hor_locate_gathered(const hor_layout* L, int64_t slice, int p, int64_t e,
                             int* shard, int64_t* k);
 void hor_locate_fused_many(const hor_layout* L, int64_t n, const int* s, const int64_t* j,
