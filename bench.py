@@ -48,6 +48,9 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default="large_hsdp")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the other workloads' step (reported under per_workload)")
+    ap.add_argument("--per-workload-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -513,11 +516,17 @@ def run_gpu(args, wl):
     if not args.no_e2e:
         e2e = run_e2e(args, unit, calls, step_bytes, world, dev)
 
-    pipeline = None
-    if args.pipeline:
+    per_workload = None
+    want_per = not args.no_per_workload and args.scale == 1.0 and wl.key == "large_hsdp"
+    if args.pipeline or want_per:
         unit.close()
         del unit
         torch.cuda.empty_cache()
+    if want_per:
+        per_workload = run_per_workload(args, dev, peak)
+
+    pipeline = None
+    if args.pipeline:
         pipeline = run_pipeline(args, wl, d0, dev)
 
     cpu = None
@@ -539,12 +548,82 @@ def run_gpu(args, wl):
                 "kernels": kernels, "kernels_outside_step": extra,
                 "roofline": roofline, "roofline_second": roofline_2,
                 "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches}
+        if per_workload:
+            line["per_workload"] = per_workload
         if pipeline:
             line["pipeline"] = pipeline
         print(json.dumps(line), flush=True)
-    if not args.pipeline:
+    if not (args.pipeline or want_per):
         unit.close()
     return 0
+
+
+PER_WORKLOADS = ["hsdp_2x4_llama", "ragged_fsdp", "pure_tp_compat"]
+
+
+def run_per_workload(args, dev, peak):
+    """The same step on the other full-size workloads (HSDP (2,4) Llama
+    layer, ragged-heavy FSDP, pure-TP compat), each on its own unit after the
+    headline workload's unit is freed: per kernel µs, algorithmic GB/s and
+    fraction of the measured peak, and the step's GB/s, with the clocks seen
+    while they ran. W warm-up steps, then K timed steps; workloads smaller
+    than 4x L2 flush it between steps, outside the step's events."""
+    import torch
+
+    from hsdp_sharded_parameter_gb300 import capi as C
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+    from hsdp_sharded_parameter_gb300.runtime import HsdpUnit
+
+    K = max(1, args.per_workload_steps)
+    stream = torch.cuda.current_stream()
+    out = {}
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for key in PER_WORKLOADS:
+        wl = WL.WORKLOADS[key]
+        plan = C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).upload()
+        unit = HsdpUnit(plan, wl.param_dtype, wl.grad_dtype, device=dev)
+        WL.torch_fill_(unit.shards, wl.seed_params, wl.param_std, wl.param_dtype)
+        WL.torch_fill_(unit.grads, wl.seed_grads, wl.grad_std, wl.grad_dtype)
+        sizes = plan_sizes(plan)
+        sizes["slice_ag"] = plan.slice_numel(wl.param_dtype)
+        sizes["slice_f32"] = plan.slice_numel("f32")
+        kb = algorithmic_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype)
+        step_bytes = sum(kb.values())
+        flush = step_bytes < 4 * L2_BYTES
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+        calls = [lambda: unit.ag_copy_in(fuse_gather=True), unit.ag_copy_out, unit.rs_ar_reduce,
+                 lambda: unit.apply_grads("avg")]
+        for _ in range(max(3, args.warmup)):
+            for c in calls:
+                c()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+        for k in range(K):
+            if flush:
+                scratch.zero_()
+            ev[k][0].record(stream)
+            for i, c in enumerate(calls):
+                c()
+                ev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+        kernels = {}
+        for i, n in enumerate(KERNELS):
+            us = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)) / K * 1e3
+            gbs = kb[n] / (us * 1e-6) / 1e9
+            kernels[n] = {"us": round(us, 2), "bytes": kb[n], "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        step_us = sum(ev[k][0].elapsed_time(ev[k][len(calls)]) for k in range(K)) / K * 1e3
+        out[key] = {"rank_size": wl.rank_size, "shard_size": wl.shard_size, "params": wl.n_params,
+                    "elements_per_rank": sizes["N"], "steps": K, "step_us": round(step_us, 2),
+                    "step_bytes": step_bytes, "step_gbs": round(step_bytes / (step_us * 1e-6) / 1e9, 1),
+                    "l2": "flushed between steps" if flush else "working set larger than L2",
+                    "kernels": kernels}
+        unit.close()
+        plan.close()
+        del unit, scratch
+        torch.cuda.empty_cache()
+    out["clocks"] = clocks.stop()
+    return out
 
 
 def run_pipeline(args, wl, d0, dev):

@@ -1,142 +1,29 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
 benchmark times (fused copy-in + gather, copy-out, fused RS+AR, apply AVG).
 
-The forward path is checked completely with the oracle's layout: every
-gathered buffer and every full parameter, data and padding. The gradient
-sync is checked on sampled outputs the oracle computes one by one (random
-positions plus every run boundary and its neighbours), and completely for the
-properties that hold at any size (padding is +0, replicas agree)."""
+Every output byte of the step is compared with the CPU oracle: every
+gathered buffer, every full parameter, every fp32 fused region and every
+applied shard gradient, data and padding (``full_parity``: the oracle runs
+on parameter groups and column blocks of the plan, each a plan of its own,
+spread over the host cores)."""
 import gc
 
-import numpy as np
 import pytest
 import torch
 
+import full_parity as FP
 import oracle as O
 from hsdp_sharded_parameter_gb300 import capi as C
 from hsdp_sharded_parameter_gb300 import workloads as WL
 from hsdp_sharded_parameter_gb300.runtime import HsdpUnit
 
-from gpu_util import dirty, fill_, to_np
+from gpu_util import dirty, fill_
 
 pytestmark = pytest.mark.gpu
-
-N_RANDOM = 200_000
 
 
 def bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
-
-
-def data_mask(L, s, length, device):
-    """Device bool mask over a slice row of shard s: True on actual shard
-    elements, from the oracle's layout."""
-    m = torch.zeros(length, dtype=torch.bool, device=device)
-    for p in range(L.P):
-        n = L.shard_numel(p, s)
-        if n:
-            m[L.o[p]:L.o[p] + n] = True
-    return m
-
-
-def check_forward(L, unit):
-    S, P, W = L.S, L.P, L.W
-    sl = L.slice(unit.ag_dt)
-    dev = unit.device
-    masks = [data_mask(L, s, sl, dev) for s in range(S)]
-    for w in range(W):
-        d = w // S
-        for sp in range(S):
-            row = unit.ag_out[w][sp * sl:(sp + 1) * sl]
-            # padding rows and the slice tail are zero
-            assert int(bits(row)[~masks[sp]].count_nonzero()) == 0, ("ag padding", w, sp)
-            # actual rows hold shard sp of the shard-group member (d, sp)
-            for p in range(P):
-                n = L.shard_numel(p, sp)
-                if n:
-                    src = unit.shards[(d * S + sp) * P + p]
-                    assert torch.equal(bits(row[L.o[p]:L.o[p] + n]), bits(src)), ("ag data", w, sp, p)
-        for p in range(P):
-            parts = [unit.shards[(d * S + sp) * P + p] for sp in range(S)]
-            # [RAGGED §6.4]: after the gather only the logical parameter is exposed
-            assert torch.equal(bits(unit.full[w * P + p]), bits(torch.cat(parts))), ("full", w, p)
-
-
-def sample_rows(L, rng, sf):
-    """(s, j) samples over the fused region: random positions plus, for every
-    run of every shard row, its first and last element and both neighbours."""
-    s = rng.integers(0, L.S, N_RANDOM)
-    j = rng.integers(0, max(sf, 1), N_RANDOM)
-    bs, bj = [], []
-    for sh in range(L.S):
-        for p in range(L.P):
-            n = L.shard_numel(p, sh)
-            for x in (L.o[p] - 1, L.o[p], L.o[p] + 1, L.o[p] + n - 1, L.o[p] + n, L.o[p] + n + 1):
-                if 0 <= x < sf:
-                    bs.append(sh)
-                    bj.append(x)
-        for x in (sf - 1, L.sum_padded, L.sum_padded - 1):
-            if 0 <= x < sf:
-                bs.append(sh)
-                bj.append(x)
-    return np.concatenate([s, bs]).astype(np.int32), np.concatenate([j, bj]).astype(np.int64)
-
-
-def gather_grads(L, unit, p_idx, e_idx):
-    """Gradient values g_{w,p}[e] for every rank w at the sampled (p, e)
-    (padding samples get 0), as fp32 on the host, shape (n, W)."""
-    n = len(p_idx)
-    vals = np.zeros((n, L.W), np.float32)
-    dev = unit.device
-    for p in np.unique(p_idx[p_idx >= 0]):
-        sel = np.nonzero(p_idx == p)[0]
-        idx = torch.from_numpy(e_idx[sel]).to(dev)
-        cols = torch.stack([unit.grads[w * L.P + p][idx] for w in range(L.W)], dim=1)
-        vals[sel] = cols.float().cpu().numpy()
-    return vals
-
-
-def check_backward(L, unit, rng, op="avg"):
-    S, D, P, W = L.S, L.D, L.P, L.W
-    sf = L.slice("f32")
-    dev = unit.device
-    # properties over every element: padding is +0, replicas agree
-    for s in range(S):
-        mask = data_mask(L, s, sf, dev)
-        for d in range(D):
-            f = unit.fused[d * S + s]
-            assert int(bits(f)[~mask].count_nonzero()) == 0, ("fused padding", d, s)
-            if d:
-                assert torch.equal(bits(f), bits(unit.fused[s])), ("replicas differ", d, s)
-    # sampled values: the oracle folds the gathered gradients
-    s_idx, j_idx = sample_rows(L, rng, sf)
-    p_idx, e_idx = O.locate_fused(L, s_idx, j_idx)
-    exp = O.fold_nested(S, D, gather_grads(L, unit, p_idx, e_idx))
-    exp[p_idx < 0] = 0.0
-    for d in range(D):
-        got = np.zeros(len(s_idx), np.float32)
-        for s in range(S):
-            sel = np.nonzero(s_idx == s)[0]
-            got[sel] = unit.fused[d * S + s][torch.from_numpy(j_idx[sel]).to(dev)].cpu().numpy()
-        assert np.array_equal(got.view(np.uint32), exp.view(np.uint32)), ("fused values", d)
-    # applied gradients at the sampled data positions
-    keep = p_idx >= 0
-    div = W if op == "avg" else 1
-    q = O.div(exp[keep], div)
-    exp_g = O.f32_to_bf16(q) if unit.grad_dt == "bf16" else q
-    ks = j_idx[keep] - L.o[p_idx[keep]]
-    sk, pk = s_idx[keep], p_idx[keep]
-    groups = {}
-    for i, key in enumerate(zip(sk.tolist(), pk.tolist())):
-        groups.setdefault(key, []).append(i)
-    for d in range(D):
-        got = np.zeros(len(ks), exp_g.dtype)
-        for (s, p), rows in groups.items():
-            rows = np.asarray(rows)
-            idx = torch.from_numpy(ks[rows]).to(dev)
-            got[rows] = to_np(unit.shard_grads[(d * S + s) * P + p][idx])
-        assert np.array_equal(got.view(np.uint8), exp_g.view(np.uint8)), ("applied grads", d)
-    return len(s_idx)
 
 
 def build(key, with_unfused=False):
@@ -164,27 +51,19 @@ def free(*objs):
 @pytest.mark.parametrize("key", ["hsdp_2x4_llama", "ragged_fsdp", "pure_tp_compat", "large_hsdp"])
 def test_workload_full_size(key):
     wl, plan, L, unit = build(key)
-    rng = np.random.default_rng(wl.index)
     unit.step(op="avg", fuse_gather=True)
     torch.cuda.synchronize()
-    check_forward(L, unit)
-    n = check_backward(L, unit, rng, "avg")
-    assert n >= N_RANDOM
+    assert FP.check_unit(L, unit, "avg") >= 1
     free(unit, plan)
 
 
 @pytest.mark.parametrize("key", ["ragged_fsdp", "large_hsdp"])
 def test_direct_unshard_full_size(key):
-    # all three forward steps in one pass must give the same full parameters
+    # all three forward steps in one pass give the oracle's full parameters
     wl, plan, L, unit = build(key)
     unit.unshard_direct()
     torch.cuda.synchronize()
-    S, P = L.S, L.P
-    for w in range(L.W):
-        d = w // S
-        for p in range(P):
-            parts = [unit.shards[(d * S + sp) * P + p] for sp in range(S)]
-            assert torch.equal(bits(unit.full[w * P + p]), bits(torch.cat(parts))), (w, p)
+    FP.check_unit(L, unit, forward=True, gathered=False, backward=False)
     free(unit, plan)
 
 
@@ -194,7 +73,7 @@ def test_pure_tp_sum_op():
     assert plan.comm_calls() == (0, 8)
     unit.reduce_grads("sum")
     torch.cuda.synchronize()
-    check_backward(L, unit, np.random.default_rng(9), "sum")
+    FP.check_unit(L, unit, "sum", forward=False)
     free(unit, plan)
 
 
@@ -217,8 +96,7 @@ def test_offsets_beyond_32_bits():
         dirty(bufs)
     unit.step(op="avg", fuse_gather=True)
     torch.cuda.synchronize()
-    check_forward(L, unit)
-    check_backward(L, unit, np.random.default_rng(6003), "avg")
+    FP.check_unit(L, unit, "avg")
     # the unfused path and the direct unshard give the same bits
     fused = [t.clone() for t in unit.shard_grads]
     dirty(unit.shard_grads)
