@@ -678,7 +678,7 @@ def run_pipeline(args, wl, d0, dev):
             t_sync = timed(lambda: [units[L].reduce_grads_unfused("avg") for L in reversed(range(n))])
         res = {"sync_only_ms": round(t_sync, 3), "serial_ms": round(t_comp + t_sync, 3)}
         # sync kernels on the whole GPU (0) or on a capped number of blocks
-        for cap in (0, 32, 64, 128):
+        for cap in (0, 64, 96, 112, 128):
             t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap).run(compute))
             hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
             res[f"comm_blocks_{cap}"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}

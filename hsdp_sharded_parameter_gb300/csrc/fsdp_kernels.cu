@@ -61,7 +61,9 @@ constexpr int kMaxStagedSources = 32;
 // (pure-TP layer, 8: 0.855 -> 0.903 of the measured copy peak), and with 2
 // when there are at most 8 sources (HSDP (2,4): 0.948 -> 0.961); the (2,8)
 // mesh's 16 sources measured slower with it (0.939 -> 0.924).
-constexpr size_t kFanImgBytes = kStepElems * sizeof(float);  // one step of fp32
+// One reduce step of RG granules per lane (RG * 256 elements) of fp32.
+template <int RG>
+__host__ __device__ constexpr size_t fan_img_bytes() { return (size_t)RG * kStepElems * sizeof(float); }
 // The unfused AllReduce fans out from 4 replicas on (pure-TP, 8: 0.84 ->
 // 0.90; with 2 it measured slower, 0.878 -> 0.841).
 template <int KIND, int NS, int ND>
@@ -567,28 +569,50 @@ __device__ __forceinline__ void apply_body(const KArgs& a) {
 #pragma unroll
                 for (int u = 0; u < kSteps; ++u) load_raw_at(r[u], b + (uintptr_t)(u * kStepElems * 4));
             } else {
-                // fp32 source off the 16-byte grid by whole elements: lane l
-                // takes elements l, l+32, ..., l+224 of every step, so each
-                // load reads 128 contiguous bytes of the warp and needs no
-                // realignment (far fewer registers than shuffling 16-byte
-                // blocks into place); the stores follow the same mapping
-                const float* s0 = src + cur.rel0 + lane;
+                // fp32 source off the 16-byte grid by k = 1..3 whole
+                // elements: lane l loads its two aligned blocks of each step
+                // (bytes 32l .. 32l+31 past the step's aligned start), takes
+                // the third from lane l+1 by a warp shuffle (lane 31 takes
+                // lane 0's first block of the next step, or loads it on the
+                // last step: it holds the step's last elements, so it lies in
+                // the run), and keeps words k..k+7: 16-byte loads and one
+                // 16-byte store per granule instead of element-wise accesses
+                const int kw = (int)(sh >> 2);
+                const uint4* q = reinterpret_cast<const uint4*>(t0 - sh) + lane * 2;
+                uint4 b[kSteps][2];
 #pragma unroll
-                for (int u = 0; u < kSteps; ++u)
-#pragma unroll
-                    for (int i = 0; i < kGran; ++i) r[u].w[i] = __float_as_uint(__ldcs(s0 + u * kStepElems + i * 32));
+                for (int u = 0; u < kSteps; ++u) {
+                    b[u][0] = ld_stream(q + u * 64);
+                    b[u][1] = ld_stream(q + u * 64 + 1);
+                }
+                const uint4 tail = lane == 31 ? ld_stream(q + (kSteps - 1) * 64 + 2) : make_uint4(0, 0, 0, 0);
                 if (tn < total) lookup(a, tn, k, (int)sizeof(D), nxt);
-                D* d0 = dst + cur.rel0 + lane;
 #pragma unroll
-                for (int u = 0; u < kSteps; ++u)
+                for (int u = 0; u < kSteps; ++u) {
+                    // lanes 1..31 hand their first block down one lane; lane 0
+                    // hands lane 31 its first block of the next step
+                    const uint4 give = (lane == 0 && u + 1 < kSteps) ? b[u + 1 < kSteps ? u + 1 : u][0] : b[u][0];
+                    uint4 nx;
+                    nx.x = __shfl_sync(kFull, give.x, (lane + 1) & 31);
+                    nx.y = __shfl_sync(kFull, give.y, (lane + 1) & 31);
+                    nx.z = __shfl_sync(kFull, give.z, (lane + 1) & 31);
+                    nx.w = __shfl_sync(kFull, give.w, (lane + 1) & 31);
+                    if (lane == 31 && u + 1 == kSteps) nx = tail;
+                    const uint32_t wd[12] = {b[u][0].x, b[u][0].y, b[u][0].z, b[u][0].w, b[u][1].x, b[u][1].y,
+                                             b[u][1].z, b[u][1].w, nx.x,      nx.y,      nx.z,      nx.w};
+                    Raw<float> rr;
+                    if (kw == 1) {
 #pragma unroll
-                    for (int i = 0; i < kGran; ++i) {
-                        const int64_t e = u * kStepElems + i * 32;
-                        float q = __uint_as_float(r[u].w[i]);
-                        if (scale) q = scaled(q, a);
-                        if (a.accumulate) q = __fadd_rn(load_f32(d0, e), q);
-                        store_f32(d0, e, q);
+                        for (int i = 0; i < 8; ++i) rr.w[i] = wd[i + 1];
+                    } else if (kw == 2) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) rr.w[i] = wd[i + 2];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) rr.w[i] = wd[i + 3];
                     }
+                    apply_granule<D>(a, rr, dst + cur.rel0 + u * kStepElems + lane * kGran, scale);
+                }
                 cur = nxt;
                 t = tn;
                 continue;
@@ -670,31 +694,74 @@ __device__ __forceinline__ float fold_elem(const KArgs& a, const S* const* sp, i
     return total;
 }
 
+// The staged reduce works in steps of RG * 256 elements: each lane folds
+// RG granules of 8 elements per step (granule g of lane l starts at element
+// g*256 + l*8 of the step). RG = 1 on the full grid; RG = 2 on a capped
+// grid (one block per SM), where the reduce is issue-bound and the
+// per-step work (staging the pointers, checking the sources' alignment,
+// issuing the copies, stepping through the table) is then paid once per
+// 512 elements. A step that repeats the run of the step staged last in the
+// same stage slot reuses the pointers and the alignment found then (they
+// are per-run constants).
 // Per-warp shared-memory layout of the staged reduce: per stage, one window
-// of kWin 16-byte blocks per source (a warp step of 256 elements spans 32
-// blocks of bf16 or 64 of fp32, plus one when the source is shifted), then
-// the step's source and destination pointers.
-template <typename S>
+// of kWin 16-byte blocks per source (a step of RG * 256 elements spans RG *
+// 32 blocks of bf16 or RG * 64 of fp32, plus one when the source is
+// shifted), then the step's source and destination pointers.
+template <typename S, int RG = 1>
 struct Staging {
-    static constexpr int kWin = kStepElems * (int)sizeof(S) / 16 + 1;
-    __host__ __device__ static size_t window_bytes(int ns) { return (size_t)ns * kWin * 16; }
-    __host__ __device__ static size_t stage_bytes(int ns, int nd) {
+    static constexpr int kWin = RG * kStepElems * (int)sizeof(S) / 16 + 1;
+    __host__ __device__ static constexpr size_t window_bytes(int ns) { return (size_t)ns * kWin * 16; }
+    __host__ __device__ static constexpr size_t stage_bytes(int ns, int nd) {
         return window_bytes(ns) + (size_t)(ns + nd) * sizeof(void*) + 15 & ~(size_t)15;
     }
-    __host__ __device__ static size_t warp_bytes(int ns, int nd) { return 2 * stage_bytes(ns, nd); }
+    __host__ __device__ static constexpr size_t warp_bytes(int ns, int nd) { return 2 * stage_bytes(ns, nd); }
 };
 
 struct Step {
-    int64_t n, dst_off, src_off, rel;  // rel: run-relative element of lane 0's granule
+    int64_t n, dst_off, src_off, rel;  // rel: run-relative element of lane 0's first granule
     int p, row, rep;
     bool valid;
     bool fast;       // interior data step whose sources all share one 16-byte shift
     unsigned shift;  // that shift in bytes (0 = aligned)
 };
 
-// Yields a warp's steps in order: its tiles (grid stride), 8 steps each,
-// skipping steps past the end of their run. Warp-uniform.
+// What a stage slot last staged: the run's key (p, row, rep), whether its
+// sources share one 16-byte shift, and that shift. Warp-uniform.
+// Which reduces use the slot cache and the packed (f32x2) adds: both cut
+// instructions, which pays on a capped grid, where the reduce is
+// issue-bound; on the full grid (HBM-bound) they measured slower (ragged
+// layer 0.999 -> 0.912 of the copy peak with both).
+#ifndef FSDP_SLOT_CACHE_FULL
+#define FSDP_SLOT_CACHE_FULL 0
+#endif
+#ifndef FSDP_PACKED_ADDS_FULL
+#define FSDP_PACKED_ADDS_FULL 0
+#endif
+#ifndef FSDP_SLOT_CACHE_SM
+#define FSDP_SLOT_CACHE_SM 1
+#endif
+#ifndef FSDP_PACKED_ADDS_SM
+#define FSDP_PACKED_ADDS_SM 1
+#endif
+template <int RG>
+__host__ __device__ constexpr bool slot_cache() { return RG == 1 ? FSDP_SLOT_CACHE_FULL != 0 : FSDP_SLOT_CACHE_SM != 0; }
+template <int RG>
+__host__ __device__ constexpr bool packed_adds() { return RG == 1 ? FSDP_PACKED_ADDS_FULL != 0 : FSDP_PACKED_ADDS_SM != 0; }
+
+struct SlotCache {
+    int64_t dst_off = -1;
+    int p = -2, row = -1, rep = -1;
+    bool uniform = false;
+    unsigned shift = 0;
+};
+
+// Yields a warp's steps in order: its tiles (grid stride), kWarpTile /
+// (RG * 256) steps each, skipping steps past the end of their run.
+// Warp-uniform.
+template <int RG>
 struct StepGen {
+    static constexpr int kStep = RG * kStepElems, kPerTile = kWarpTile / kStep;
+    static_assert(kWarpTile % kStep == 0, "a warp tile is a whole number of reduce steps");
     int64_t t, stride, total;
     int u, k;
     Tile tile;
@@ -713,13 +780,13 @@ struct StepGen {
         s.shift = 0;
         for (;;) {
             if (t >= total) return s;
-            if (++u == kSteps) {
+            if (++u == kPerTile) {
                 t += stride;
                 u = 0;
                 if (t >= total) return s;
                 lookup(a, t, k, 4, tile);
             }
-            const int64_t rel = tile.rel0 + (int64_t)u * kStepElems;
+            const int64_t rel = tile.rel0 + (int64_t)u * kStep;
             if (rel < tile.n) {
                 s.n = tile.n;
                 s.dst_off = tile.dst_off;
@@ -755,20 +822,25 @@ struct Shape {
     }
 };
 
-// Stage one step: pointers into the stage's pointer area, and for a data
-// run with aligned destinations, each source's window via cp.async (only
-// blocks that hold bytes of the step's valid range). An interior step whose
-// sources are all 16-byte aligned copies exactly the 256 elements of each
-// source, one 16-byte block per lane per vector. Always commits one group
-// (possibly empty) so the group count stays in step with the ring.
-template <int KIND, typename S, int NS, int SIN, int ND>
-__device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage, const Shape<KIND, NS, SIN, ND>& sh) {
+// Stage one step: pointers into the stage's pointer area (unless the slot
+// holds this run's already), and for a data run with aligned destinations,
+// each source's window via cp.async (only blocks that hold bytes of the
+// step's valid range). An interior step whose sources are all 16-byte
+// aligned copies exactly the RG * 256 elements of each source, RG blocks per
+// lane per 16-byte vector. Always commits one group (possibly empty) so the
+// group count stays in step with the ring.
+template <int KIND, typename S, int NS, int SIN, int ND, int RG>
+__device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage, SlotCache& c,
+                                           const Shape<KIND, NS, SIN, ND>& sh) {
     const int lane = threadIdx.x & 31;
-    constexpr int kWin = Staging<S>::kWin;
+    constexpr int kWin = Staging<S, RG>::kWin;
+    constexpr int kStep = RG * kStepElems;
     uint4* win = reinterpret_cast<uint4*>(stage);
-    const S** sp = reinterpret_cast<const S**>(stage + Staging<S>::window_bytes(sh.ns));
-    float** dp = reinterpret_cast<float**>(stage + Staging<S>::window_bytes(sh.ns) + sh.ns * sizeof(void*));
-    if (st.valid) {
+    const S** sp = reinterpret_cast<const S**>(stage + Staging<S, RG>::window_bytes(sh.ns));
+    float** dp = reinterpret_cast<float**>(stage + Staging<S, RG>::window_bytes(sh.ns) + sh.ns * sizeof(void*));
+    const bool same = slot_cache<RG>() && st.valid && st.p == c.p && st.row == c.row && st.rep == c.rep &&
+                      st.dst_off == c.dst_off;
+    if (st.valid && !same) {
         if (st.p >= 0)
             for (int i = lane; i < sh.ns; i += 32) sp[i] = ReduceShape<KIND>::template src<S>(a, st.p, st.row, st.rep, i);
         for (int j = lane; j < sh.nd; j += 32) dp[j] = ReduceShape<KIND>::dst(a, st.row, st.rep, j) + st.dst_off;
@@ -777,28 +849,38 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
     if (st.valid && st.p >= 0 && a.vec) {
         const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(win));
         const int64_t byte0 = (st.src_off + st.rel) * (int64_t)sizeof(S);  // may precede the run: address only
-        const unsigned sh0 = (unsigned)((reinterpret_cast<uintptr_t>(sp[0]) + (uintptr_t)byte0) & 15u);
-        bool ok = true;
-        for (int i = lane; i < sh.ns; i += 32)
-            ok = ok && ((reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)byte0) & 15u) == sh0;
-        const bool uniform = __all_sync(kFull, ok);
-        if (uniform && st.rel >= 0 && st.rel + kStepElems <= st.n) {
-            // every source window starts sh0 bytes before its first element;
-            // a shifted window needs one block more, copied by lane 0
+        if (!same) {
+            // one shift for every source? (a per-run constant: steps of a run
+            // are whole multiples of 256 elements apart)
+            const unsigned sh0 = (unsigned)((reinterpret_cast<uintptr_t>(sp[0]) + (uintptr_t)byte0) & 15u);
+            bool ok = true;
+            for (int i = lane; i < sh.ns; i += 32)
+                ok = ok && ((reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)byte0) & 15u) == sh0;
+            c.uniform = __all_sync(kFull, ok);
+            c.shift = sh0;
+            c.p = st.p;
+            c.row = st.row;
+            c.rep = st.rep;
+            c.dst_off = st.dst_off;
+        }
+        if (c.uniform && st.rel >= 0 && st.rel + kStep <= st.n) {
+            // every source window starts `shift` bytes before its first
+            // element; a shifted window needs one block more, copied by lane 0
             st.fast = true;
-            st.shift = sh0;
+            st.shift = c.shift;
 #pragma unroll
             for (int i = 0; i < sh.ns; ++i) {
-                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0 - sh0;
+                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0 - c.shift + lane * 16;
+                const uint32_t s0 = sbase + (uint32_t)((i * kWin + lane) * 16);
 #pragma unroll
-                for (int v = 0; v < Raw<S>::kVec; ++v)
-                    cp_async16(sbase + (uint32_t)((i * kWin + lane + 32 * v) * 16), g + (lane + 32 * v) * 16);
-                if (sh0 != 0 && lane == 0)
-                    cp_async16(sbase + (uint32_t)((i * kWin + kWin - 1) * 16), g + (kWin - 1) * 16);
+                for (int v = 0; v < RG * Raw<S>::kVec; ++v) cp_async16(s0 + (uint32_t)(v * 32 * 16), g + v * 32 * 16);
+                if (c.shift != 0 && lane == 0)
+                    cp_async16(sbase + (uint32_t)((i * kWin + kWin - 1) * 16),
+                               reinterpret_cast<const char*>(sp[i]) + byte0 - c.shift + (kWin - 1) * 16);
             }
         } else {
             const int64_t e_lo = st.rel < 0 ? 0 : st.rel;
-            const int64_t e_hi = st.rel + kStepElems < st.n ? st.rel + kStepElems : st.n;
+            const int64_t e_hi = st.rel + kStep < st.n ? st.rel + kStep : st.n;
             for (int i = 0; i < sh.ns; ++i) {
                 const uintptr_t base = reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)(st.src_off * (int64_t)sizeof(S));
                 const uintptr_t wst = (base + (uintptr_t)(st.rel * (int64_t)sizeof(S))) & ~(uintptr_t)15;
@@ -811,14 +893,22 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
                 }
             }
         }
+    } else if (st.valid && !same) {
+        // zero runs and unaligned destinations stage no windows; the slot
+        // now holds this run's pointers
+        c.p = st.p;
+        c.row = st.row;
+        c.rep = st.rep;
+        c.dst_off = st.dst_off;
+        c.uniform = false;
     }
     cp_async_commit();
 }
 
-// Reads a lane's 8 elements of source i from its staged window.
-template <typename S>
-__device__ __forceinline__ void read_window(const uint4* win, int i, int lane, unsigned sh, Raw<S>& r) {
-    const uint4* w = win + i * Staging<S>::kWin + lane * Raw<S>::kVec;
+// Reads granule g of a lane's 8 elements of source i from its staged window.
+template <typename S, int RG>
+__device__ __forceinline__ void read_window(const uint4* win, int i, int lane, int g, unsigned sh, Raw<S>& r) {
+    const uint4* w = win + i * Staging<S, RG>::kWin + (g * 32 + lane) * Raw<S>::kVec;
     if (sh == 0) {
 #pragma unroll
         for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, w[v]);
@@ -831,33 +921,39 @@ __device__ __forceinline__ void read_window(const uint4* win, int i, int lane, u
     }
 }
 
-// Interior step whose sources share one shift: every lane's granule is
-// full; source i of lane l starts `shift` bytes into window block l*kVec.
-template <bool SHIFTED, typename S, int NS, int SIN, int ND, int KIND>
-__device__ __forceinline__ void fold_fast(const uint4* win, int lane, unsigned shift,
+// x[2k..2k+1] += y[2k..2k+1] as packed pairs: each element one IEEE binary32
+// round-to-nearest-even addition, as __fadd_rn would do it.
+__device__ __forceinline__ void add_pairs(float (&x)[8], const float (&y)[8]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint64_t a = (uint64_t)__float_as_uint(x[2 * k]) | ((uint64_t)__float_as_uint(x[2 * k + 1]) << 32);
+        const uint64_t b = (uint64_t)__float_as_uint(y[2 * k]) | ((uint64_t)__float_as_uint(y[2 * k + 1]) << 32);
+        asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(b));
+        x[2 * k] = __uint_as_float((uint32_t)a);
+        x[2 * k + 1] = __uint_as_float((uint32_t)(a >> 32));
+    }
+}
+
+// Interior step whose sources share one shift: granule g of the lane is
+// full; source i of lane l starts `shift` bytes into its window's block
+// (g*32 + l)*kVec.
+template <bool SHIFTED, typename S, int RG, int NS, int SIN, int ND, int KIND>
+__device__ __forceinline__ void fold_fast(const uint4* win, int lane, int g, unsigned shift,
                                           const Shape<KIND, NS, SIN, ND>& sh, float (&total)[8]) {
 #pragma unroll
     for (int d = 0; d < sh.d_out; ++d) {
         float part[8];
 #pragma unroll
         for (int s = 0; s < sh.s_in; ++s) {
-            const uint4* w = win + (d * sh.s_in + s) * Staging<S>::kWin + lane * Raw<S>::kVec;
             Raw<S> r;
-            if (SHIFTED) {
-                uint4 blk[Raw<S>::kVec + 1];
-#pragma unroll
-                for (int v = 0; v <= Raw<S>::kVec; ++v) blk[v] = w[v];
-#pragma unroll
-                for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, funnel(blk[v], blk[v + 1], shift));
-            } else {
-#pragma unroll
-                for (int v = 0; v < Raw<S>::kVec; ++v) put(r.w + 4 * v, w[v]);
-            }
+            read_window<S, RG>(win, d * sh.s_in + s, lane, g, SHIFTED ? shift : 0u, r);
             float x[8];
             widen(r, x);
             if (s == 0) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part[e] = x[e];
+            } else if constexpr (packed_adds<RG>()) {
+                add_pairs(part, x);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part[e] = __fadd_rn(part[e], x[e]);
@@ -866,6 +962,8 @@ __device__ __forceinline__ void fold_fast(const uint4* win, int lane, unsigned s
         if (d == 0) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) total[e] = part[e];
+        } else if constexpr (packed_adds<RG>()) {
+            add_pairs(total, part);
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(total[e], part[e]);
@@ -873,103 +971,116 @@ __device__ __forceinline__ void fold_fast(const uint4* win, int lane, unsigned s
     }
 }
 
-template <int KIND, typename S, int NS, int SIN, int ND>
+template <int KIND, typename S, int NS, int SIN, int ND, int RG>
 __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, const char* stage,
                                              const Shape<KIND, NS, SIN, ND>& sh, uint4* img, int& parity) {
     if (!st.valid) return;
     const int lane = threadIdx.x & 31;
     const uint4* win = reinterpret_cast<const uint4*>(stage);
-    const S* const* sp = reinterpret_cast<const S* const*>(stage + Staging<S>::window_bytes(sh.ns));
-    float* const* dp = reinterpret_cast<float* const*>(stage + Staging<S>::window_bytes(sh.ns) + sh.ns * sizeof(void*));
-    const int64_t rel = st.rel + lane * kGran;
+    const S* const* sp = reinterpret_cast<const S* const*>(stage + Staging<S, RG>::window_bytes(sh.ns));
+    float* const* dp =
+        reinterpret_cast<float* const*>(stage + Staging<S, RG>::window_bytes(sh.ns) + sh.ns * sizeof(void*));
+    constexpr size_t kImg = fan_img_bytes<RG>();
     const bool scale = a.div != 1.0f;
     if (st.fast) {
-        float total[8];
-        if (st.shift == 0)
-            fold_fast<false, S>(win, lane, 0u, sh, total);
-        else
-            fold_fast<true, S>(win, lane, st.shift, sh, total);
-        if (scale) {
+        Raw<float> o[RG];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
+        for (int g = 0; g < RG; ++g) {
+            float total[8];
+            if (st.shift == 0)
+                fold_fast<false, S, RG>(win, lane, g, 0u, sh, total);
+            else
+                fold_fast<true, S, RG>(win, lane, g, st.shift, sh, total);
+            if (scale) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
+            }
+            narrow(total, o[g]);
         }
-        Raw<float> o;
-        narrow(total, o);
         if constexpr (fan_out<KIND, NS, ND>()) {
-            // the step's 256 results as one image (two per warp, in turn;
-            // an image is rewritten only after the bulk stores of two fast
-            // steps ago have read it), written to every replica by lane 0
-            uint4* im = img + parity * (int)(kFanImgBytes / 16);
+            // the step's results as one image (two per warp, in turn; an
+            // image is rewritten only after the bulk stores of two fast steps
+            // ago have read it), written to every replica by lane 0
+            uint4* im = img + parity * (int)(kImg / 16);
             if (lane == 0) bulk_wait_read_1();
             __syncwarp();
-            im[2 * lane] = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
-            im[2 * lane + 1] = make_uint4(o.w[4], o.w[5], o.w[6], o.w[7]);
+#pragma unroll
+            for (int g = 0; g < RG; ++g) {
+                im[2 * (g * 32 + lane)] = make_uint4(o[g].w[0], o[g].w[1], o[g].w[2], o[g].w[3]);
+                im[2 * (g * 32 + lane) + 1] = make_uint4(o[g].w[4], o[g].w[5], o[g].w[6], o[g].w[7]);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(im));
 #pragma unroll
-                for (int j = 0; j < sh.nd; ++j) bulk_store(dp[j] + st.rel, s, (uint32_t)kFanImgBytes);
+                for (int j = 0; j < sh.nd; ++j) bulk_store(dp[j] + st.rel, s, (uint32_t)kImg);
                 bulk_commit();
             }
             parity ^= 1;
         } else {
 #pragma unroll
-            for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
+            for (int j = 0; j < sh.nd; ++j)
+#pragma unroll
+                for (int g = 0; g < RG; ++g) store_raw(dp[j] + st.rel + g * kStepElems + lane * kGran, o[g]);
         }
         return;
     }
-    if (rel >= st.n || rel + kGran <= 0) return;
-    if (a.vec && rel >= 0 && rel + kGran <= st.n) {
-        float total[8];
-        if (st.p < 0) {
+#pragma unroll 1
+    for (int g = 0; g < RG; ++g) {
+        const int64_t rel = st.rel + g * kStepElems + lane * kGran;
+        if (rel >= st.n || rel + kGran <= 0) continue;
+        if (a.vec && rel >= 0 && rel + kGran <= st.n) {
+            float total[8];
+            if (st.p < 0) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) total[e] = 0.0f;
-        } else {
-            for (int d = 0; d < sh.d_out; ++d) {
-                float part[8];
-                for (int s = 0; s < sh.s_in; ++s) {
-                    const int i = d * sh.s_in + s;
-                    const unsigned shift = (unsigned)((reinterpret_cast<uintptr_t>(sp[i]) +
-                                                       (uintptr_t)((st.src_off + st.rel) * (int64_t)sizeof(S))) & 15u);
-                    Raw<S> r;
-                    read_window<S>(win, i, lane, shift, r);
-                    float x[8];
-                    widen(r, x);
-                    if (s == 0) {
+                for (int e = 0; e < 8; ++e) total[e] = 0.0f;
+            } else {
+                for (int d = 0; d < sh.d_out; ++d) {
+                    float part[8];
+                    for (int s = 0; s < sh.s_in; ++s) {
+                        const int i = d * sh.s_in + s;
+                        const unsigned shift = (unsigned)((reinterpret_cast<uintptr_t>(sp[i]) +
+                                                           (uintptr_t)((st.src_off + st.rel) * (int64_t)sizeof(S))) & 15u);
+                        Raw<S> r;
+                        read_window<S, RG>(win, i, lane, g, shift, r);
+                        float x[8];
+                        widen(r, x);
+                        if (s == 0) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) part[e] = x[e];
+                            for (int e = 0; e < 8; ++e) part[e] = x[e];
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) part[e] = __fadd_rn(part[e], x[e]);
+                        }
+                    }
+                    if (d == 0) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) total[e] = part[e];
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) part[e] = __fadd_rn(part[e], x[e]);
+                        for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(total[e], part[e]);
                     }
                 }
-                if (d == 0) {
+                if (scale) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) total[e] = part[e];
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(total[e], part[e]);
+                    for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
                 }
             }
-            if (scale) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
+            Raw<float> o;
+            narrow(total, o);
+            for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
+        } else {
+            const int64_t lo = rel < 0 ? 0 : rel;
+            const int64_t hi = rel + kGran < st.n ? rel + kGran : st.n;
+            for (int64_t e = lo; e < hi; ++e) {
+                float v = 0.0f;
+                if (st.p >= 0) {
+                    v = fold_elem<KIND, S>(a, sp, st.src_off + e);
+                    if (scale) v = scaled(v, a);
+                }
+                for (int j = 0; j < sh.nd; ++j) dp[j][e] = v;
             }
-        }
-        Raw<float> o;
-        narrow(total, o);
-        for (int j = 0; j < sh.nd; ++j) store_raw(dp[j] + rel, o);
-    } else {
-        const int64_t lo = rel < 0 ? 0 : rel;
-        const int64_t hi = rel + kGran < st.n ? rel + kGran : st.n;
-        for (int64_t e = lo; e < hi; ++e) {
-            float v = 0.0f;
-            if (st.p >= 0) {
-                v = fold_elem<KIND, S>(a, sp, st.src_off + e);
-                if (scale) v = scaled(v, a);
-            }
-            for (int j = 0; j < sh.nd; ++j) dp[j][e] = v;
         }
     }
 }
@@ -977,32 +1088,36 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
 // Two-stage ring per warp: while step i is folded from shared memory, the
 // copies of step i+1 are in flight. Each lane waits for its own copies;
 // __syncwarp then makes every lane's copies visible to the whole warp.
-template <int KIND, typename S, int NS, int SIN, int ND>
+template <int KIND, typename S, int NS, int SIN, int ND, int RG = 1>
 __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
     extern __shared__ __align__(16) char smem_raw[];
     const Shape<KIND, NS, SIN, ND> sh(a);
-    const size_t sb = Staging<S>::stage_bytes(sh.ns, sh.nd);
+    const size_t sb = Staging<S, RG>::stage_bytes(sh.ns, sh.nd);
     constexpr bool kFan = fan_out<KIND, NS, ND>();
-    char* base = smem_raw + (threadIdx.x >> 5) * (2 * sb + (kFan ? 2 * kFanImgBytes : 0));
+    char* base = smem_raw + (threadIdx.x >> 5) * (2 * sb + (kFan ? 2 * fan_img_bytes<RG>() : 0));
     char* here = base;        // stage of the step being folded
     char* there = base + sb;  // stage of the step in flight
+    SlotCache c_here, c_there;
     uint4* img = kFan ? reinterpret_cast<uint4*>(base + 2 * sb) : nullptr;  // fan-out images
     int parity = 0;
-    StepGen gen;
+    StepGen<RG> gen;
     gen.init(a);
     Step cur = gen.next(a);
-    stage_step<KIND, S>(a, cur, here, sh);
+    stage_step<KIND, S, NS, SIN, ND, RG>(a, cur, here, c_here, sh);
     while (cur.valid) {
         Step nxt = gen.next(a);
-        stage_step<KIND, S>(a, nxt, there, sh);
+        stage_step<KIND, S, NS, SIN, ND, RG>(a, nxt, there, c_there, sh);
         cp_async_wait1();
         __syncwarp();
-        consume_step<KIND, S>(a, cur, here, sh, img, parity);
+        consume_step<KIND, S, NS, SIN, ND, RG>(a, cur, here, sh, img, parity);
         __syncwarp();
         cur = nxt;
         char* t = here;
         here = there;
         there = t;
+        const SlotCache tc = c_here;
+        c_here = c_there;
+        c_there = tc;
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
     // bulk stores must have read the images before the block exits
@@ -1106,6 +1221,45 @@ __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_reduc
 template <int NS>
 __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_AR, float, NS, 1, NS>(a);
+}
+// The same reduces on a capped grid (fsdp_plan_set_grid_limit): one block
+// per SM, as many warps as the SM's shared memory holds staging rings for
+// (11 to 23 on the common meshes), so a few SMs keep as many bytes in
+// flight as many SMs do with the 4-warp blocks. On one GB300, cp.async
+// reads from one 1024-thread block per SM reach 130-180 GB/s per SM, and 48
+// SMs 6.3-6.7 TB/s; a 4-warp block keeps ~34 KB in flight and reached ~30
+// GB/s per SM. The block's warp count is fixed at compile time for the
+// compiled meshes and is an upper bound for the others (the launch then
+// picks it). These run 512-element steps (kSmRG granules per lane).
+constexpr size_t kSmBlockSmem = 220 * 1024;
+// Steps of 512 elements (two granules per lane) on a capped grid.
+constexpr int kSmRG = 2;
+template <int KIND, typename S, int NS, int ND>
+__host__ __device__ constexpr size_t staged_warp_bytes() {
+    return Staging<S, kSmRG>::warp_bytes(NS, ND) + (fan_out<KIND, NS, ND>() ? 2 * fan_img_bytes<kSmRG>() : 0);
+}
+// Warps of the one-block-per-SM reduce: as many as the shared memory holds,
+// at most 16 (the fold keeps up to ~128 registers per thread; more warps
+// would force spills).
+constexpr int kSmMaxWarps = 16;
+template <int KIND, typename S, int NS, int ND>
+__host__ __device__ constexpr int sm_warps() {
+    return NS == 0 ? 8
+                   : (kSmBlockSmem / staged_warp_bytes<KIND, S, NS, ND>() > kSmMaxWarps
+                          ? kSmMaxWarps
+                          : (int)(kSmBlockSmem / staged_warp_bytes<KIND, S, NS, ND>()));
+}
+template <typename S, int NS, int SIN, int ND>
+__global__ void __launch_bounds__(sm_warps<K_RSAR, S, NS, ND>() * 32, 1) rs_ar_reduce_sm_kernel(const KArgs a) {
+    staged_reduce_body<K_RSAR, S, NS, SIN, ND, kSmRG>(a);
+}
+template <typename S, int NS>
+__global__ void __launch_bounds__(sm_warps<K_RS, S, NS, 1>() * 32, 1) rs_reduce_sm_kernel(const KArgs a) {
+    staged_reduce_body<K_RS, S, NS, NS, 1, kSmRG>(a);
+}
+template <int NS>
+__global__ void __launch_bounds__(sm_warps<K_AR, float, NS, NS>() * 32, 1) ar_reduce_sm_kernel(const KArgs a) {
+    staged_reduce_body<K_AR, float, NS, 1, NS, kSmRG>(a);
 }
 template <typename S>
 __global__ void __launch_bounds__(kThreads) rs_ar_reduce_wide_kernel(const KArgs a) {
@@ -1290,12 +1444,29 @@ int ar_grid(bool) { return FSDP_GRID_RSAR; }
 template <typename S, typename F>
 cudaError_t go_staged(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan = false,
                       int per_sm = -1) {
-    const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * kFanImgBytes : 0);
+    const size_t per_warp = Staging<S>::warp_bytes(ns, nd) + (fan ? 2 * fan_img_bytes<1>() : 0);
     const int policy = FSDP_GRID_STAGED > 0 ? FSDP_GRID_STAGED : a.staged_blocks;
     // a staged reduce over a table with a tile -> run map takes many waves
     // even when short (2000-parameter layer: fused reduce 0.927 -> 0.996)
     return go(kernel, a, st, kStagedWarps * 32, kStagedWarps * per_warp, per_sm >= 0 ? per_sm : policy, policy,
               true);
+}
+
+// A staged reduce on a capped grid: one block per SM with `warps_max` warps
+// (fewer if their staging rings do not fit), at most a.max_grid blocks.
+template <typename S, typename F>
+cudaError_t go_sm(F kernel, const KArgs& a, cudaStream_t st, int ns, int nd, bool fan, int warps_max) {
+    const size_t per_warp = Staging<S, kSmRG>::warp_bytes(ns, nd) + (fan ? 2 * fan_img_bytes<kSmRG>() : 0);
+    int warps = (int)(kSmBlockSmem / per_warp);
+    if (warps > warps_max) warps = warps_max;
+    if (warps < 1) warps = 1;
+    const size_t smem = (size_t)warps * per_warp;
+    blocks_per_sm(reinterpret_cast<const void*>(kernel), warps * 32, smem);  // raises the smem limit once
+    const int64_t want = (a.ntiles * a.reps + warps - 1) / warps;
+    const int64_t cap = a.max_grid > 0 ? a.max_grid : sm_count();
+    const int grid = (int)(want < cap ? want : cap);
+    kernel<<<grid, warps * 32, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 // The staged reduce fits when its per-block shared memory stays well inside
@@ -1332,6 +1503,23 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return sf ? go(rs_copy_in_kernel<float>, a, st)
                       : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);
         case K_RSAR:
+            if (a.max_grid > 0 && (sf ? staged_fits<float>(a.W, a.D) : staged_fits<uint16_t>(a.W, a.D))) {
+                if (sf) {
+                    if (a.W == 4 && a.S == 4)
+                        return go_sm<float>(rs_ar_reduce_sm_kernel<float, 4, 4, 1>, a, st, 4, 1, false,
+                                            sm_warps<K_RSAR, float, 4, 1>());
+                    return go_sm<float>(rs_ar_reduce_sm_kernel<float, 0, 0, 0>, a, st, a.W, a.D, false,
+                                        sm_warps<K_RSAR, float, 0, 0>());
+                }
+#define FSDP_RSAR_SM(W_, S_)                                                                                    \
+    if (a.W == W_ && a.S == S_)                                                                                 \
+        return go_sm<uint16_t>(rs_ar_reduce_sm_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, W_ / S_,           \
+                               fan_out<K_RSAR, W_, W_ / S_>(), sm_warps<K_RSAR, uint16_t, W_, W_ / S_>());
+                FSDP_RSAR_SM(16, 8) FSDP_RSAR_SM(8, 4) FSDP_RSAR_SM(8, 8) FSDP_RSAR_SM(8, 1) FSDP_RSAR_SM(4, 4)
+#undef FSDP_RSAR_SM
+                return go_sm<uint16_t>(rs_ar_reduce_sm_kernel<uint16_t, 0, 0, 0>, a, st, a.W, a.D, false,
+                                       sm_warps<K_RSAR, uint16_t, 0, 0>());
+            }
             if (sf) {
                 if (!staged_fits<float>(a.W, a.D)) return go(rs_ar_reduce_wide_kernel<float>, a, st);
                 if (a.W == 4 && a.S == 4)
@@ -1353,6 +1541,17 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             if (a.S == 1)
                 return sf ? go(rs_reduce_copy_kernel<float>, a, st)
                           : go(rs_reduce_copy_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_COPY);
+            if (a.max_grid > 0 && (sf ? staged_fits<float>(a.S, 1) : staged_fits<uint16_t>(a.S, 1))) {
+                if (sf) return go_sm<float>(rs_reduce_sm_kernel<float, 0>, a, st, a.S, 1, false, sm_warps<K_RS, float, 0, 1>());
+                if (a.S == 8)
+                    return go_sm<uint16_t>(rs_reduce_sm_kernel<uint16_t, 8>, a, st, 8, 1, false,
+                                           sm_warps<K_RS, uint16_t, 8, 1>());
+                if (a.S == 4)
+                    return go_sm<uint16_t>(rs_reduce_sm_kernel<uint16_t, 4>, a, st, 4, 1, false,
+                                           sm_warps<K_RS, uint16_t, 4, 1>());
+                return go_sm<uint16_t>(rs_reduce_sm_kernel<uint16_t, 0>, a, st, a.S, 1, false,
+                                       sm_warps<K_RS, uint16_t, 0, 1>());
+            }
             if (sf)
                 return staged_fits<float>(a.S, 1)
                            ? go_staged<float>(rs_reduce_kernel<float, 0>, a, st, a.S, 1, false, rs_grid(a.S))
@@ -1363,6 +1562,15 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return go_staged<uint16_t>(rs_reduce_kernel<uint16_t, 0>, a, st, a.S, 1, false, rs_grid(a.S));
         case K_AR:
             if (!staged_fits<float>(a.D, a.D)) return go(ar_reduce_wide_kernel, a, st);
+            if (a.max_grid > 0) {
+                if (a.D == 2)
+                    return go_sm<float>(ar_reduce_sm_kernel<2>, a, st, 2, 2, fan_out<K_AR, 2, 2>(),
+                                        sm_warps<K_AR, float, 2, 2>());
+                if (a.D == 8)
+                    return go_sm<float>(ar_reduce_sm_kernel<8>, a, st, 8, 8, fan_out<K_AR, 8, 8>(),
+                                        sm_warps<K_AR, float, 8, 8>());
+                return go_sm<float>(ar_reduce_sm_kernel<0>, a, st, a.D, a.D, false, sm_warps<K_AR, float, 0, 0>());
+            }
             if (a.D == 2)
                 return go_staged<float>(ar_reduce_kernel<2>, a, st, 2, 2, fan_out<K_AR, 2, 2>(),
                                         ar_grid(fan_out<K_AR, 2, 2>()));

@@ -156,8 +156,10 @@ class BackwardPipeline:
 
     def __init__(self, units, op="avg", fused=False, comm_blocks=0, sync_priority=-1):
         """comm_blocks > 0 caps the thread blocks of every sync kernel the
-        pipeline issues (fsdp_plan_set_grid_limit), leaving the other SMs to
-        the backward compute. sync_priority is the sync streams' priority:
+        pipeline issues on its sync streams (fsdp_plan_set_grid_limit; the
+        reduces then run one block per SM), leaving the other SMs to the
+        backward compute; the applies on the compute stream keep the whole
+        GPU. sync_priority is the sync streams' priority:
         -1 (high, the default) places their blocks as soon as SMs free up;
         0 (the compute stream's) lets compute blocks go first."""
         self.units = list(units)
@@ -174,7 +176,10 @@ class BackwardPipeline:
         # unfused results are already scaled by the collectives (AVG);
         # the fused buffer holds the raw sum
         op = self.op if self.fused else "sum"
+        # apply runs on the compute stream: the whole GPU, not the sync cap
+        u.plan.set_grid_limit(0)
         C.fsdp_apply_grads(u.plan, u.b_fused, op, u.b_shard_grads, False, stream)
+        u.plan.set_grid_limit(self.comm_blocks)
         self.log.append(("apply", L))
 
     def run(self, backward_compute):
