@@ -292,7 +292,37 @@ def cpu_baseline(wl, target_s):
             "sample": (f"one full step (copy-in, gather, copy-out, RS copy-in + fused RS/AR sum, "
                        f"apply AVG) of the oracle on the same mesh and parameter list with every "
                        f"dim 0 scaled by {f:.3g} ({sum(a * b for a, b in zip(d0, wl.inner))} "
-                       f"elements per rank, {nbytes / 1e9:.3f} GB algorithmic), single thread")}
+                       f"elements per rank, {nbytes / 1e9:.3f} GB algorithmic), single thread"),
+            "_sample": (f, L, shards, grads, nbytes)}
+
+
+def cpu_baseline_mt(wl, sample):
+    """The same sample on every host core: the -fopenmp build of the oracle's
+    source (loops over ranks, parameters and shard rows split across
+    threads; every output byte equal to the oracle's). Reported beside the
+    single-thread baseline, not a target."""
+    import oracle as O
+    from oracle import build as OB
+
+    f, _, shards, grads, nbytes = sample
+    try:
+        OB.build(threaded=True)
+    except Exception as e:  # no OpenMP in the host compiler
+        return {"unavailable": f"no -fopenmp build of the oracle: {e}"}
+    cores = os.cpu_count() or 1
+    O.use_threaded(True)
+    try:
+        d0, inner = scaled_workload(wl, f)
+        L = O.Layout(d0, inner, wl.rank_size, wl.shard_size)
+        oracle_step(L, wl, shards, grads)  # warm the thread pool
+        t0 = time.perf_counter()
+        oracle_step(L, wl, shards, grads)
+        dt = time.perf_counter() - t0
+    finally:
+        O.use_threaded(False)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle source, -fopenmp build (same bytes as the oracle)", "seconds": round(dt, 3),
+            "sample": f"the single-thread baseline's sample, {cores} threads"}
 
 
 def run_reference(args, wl):
@@ -529,9 +559,10 @@ def run_gpu(args, wl):
     if args.pipeline:
         pipeline = run_pipeline(args, wl, d0, dev)
 
-    cpu = None
+    cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_seconds)
+        cpu_mt = cpu_baseline_mt(wl, cpu.pop("_sample"))
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -547,7 +578,8 @@ def run_gpu(args, wl):
                            "parallelism": f"{world} independent unit(s), one per GPU"},
                 "kernels": kernels, "kernels_outside_step": extra,
                 "roofline": roofline, "roofline_second": roofline_2,
-                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches}
+                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "cpu_baseline_mt": cpu_mt,
+                "gpu_launches": launches}
         if per_workload:
             line["per_workload"] = per_workload
         if pipeline:

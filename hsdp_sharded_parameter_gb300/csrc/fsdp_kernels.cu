@@ -1196,16 +1196,24 @@ __device__ __forceinline__ void direct_reduce_body(const KArgs& a) {
 // ----------------------------------------------------------- entry kernels
 // One named kernel per C-ABI call (the names show in profiles).
 
+// Minimum resident blocks per SM the copy and apply kernels are compiled
+// for (caps their registers: 2 -> 128, 3 -> 85 per thread).
+#ifndef FSDP_COPY_MINB
+#define FSDP_COPY_MINB 1
+#endif
+#ifndef FSDP_APPLY_MINB
+#define FSDP_APPLY_MINB 1
+#endif
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D, true>(a); }
+__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D, true>(a); }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ag_gather_kernel(const KArgs a) { copy_body<K_GATHER, T, T, true>(a); }
 template <typename T>
-__global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
+__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
+__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
 // The unfused ReduceScatter over a shard group of one rank: a widening copy
 // (the sum of one term, divided by 1).
 template <typename S>
@@ -1273,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads) ar_reduce_wide_kernel(const KArgs a)
     direct_reduce_body<K_AR, float>(a);
 }
 template <typename D>
-__global__ void __launch_bounds__(kThreads) apply_grads_kernel(const KArgs a) { apply_body<D>(a); }
+__global__ void __launch_bounds__(kThreads, FSDP_APPLY_MINB) apply_grads_kernel(const KArgs a) { apply_body<D>(a); }
 
 // ------------------------------------------------------------------ launch
 
@@ -1361,6 +1369,12 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 #ifndef FSDP_GRID_COPY_SHIFTED
 #define FSDP_GRID_COPY_SHIFTED 16
 #endif
+// Copy-out over a table with a tile -> run map (thousands of runs), many
+// waves: 32 (2000-parameter layer, timed inside the step: one wave 0.94,
+// 16: 0.960, 32: 0.965, 128: 0.899).
+#ifndef FSDP_GRID_COPY_MAPPED
+#define FSDP_GRID_COPY_MAPPED 32
+#endif
 #ifndef FSDP_GRID_MULTI
 #define FSDP_GRID_MULTI 256
 #endif
@@ -1390,9 +1404,33 @@ int blocks_per_sm(const void* fn, int threads, size_t smem) {
 // fallback_per_sm: blocks per SM when the launch stays at one wave (0 = as
 // many as fit). map_waves: a table with a tile -> run map is exempt from
 // the one-wave rule below.
+// Copy and apply launches over a table with a tile -> run map take many
+// waves too when set (as the staged reduces do). Off by default: the
+// copy-out, the direct unshard and the one-destination copy-in pass it
+// themselves (2000-parameter layer, timed inside the step: copy-out 0.94 ->
+// 0.965 with its own grid, one-destination copy-in 0.930 -> 0.941; unshard
+// timed alone 0.91 -> 0.924); the apply measured slower with it (0.941 ->
+// 0.934).
+#ifndef FSDP_COPY_MAP_WAVES
+#define FSDP_COPY_MAP_WAVES 0
+#endif
+#ifndef FSDP_AGOUT_MAP_WAVES
+#define FSDP_AGOUT_MAP_WAVES 1
+#endif
+#ifndef FSDP_OWN_MAP_WAVES
+#define FSDP_OWN_MAP_WAVES 1
+#endif
+#ifndef FSDP_UNSHARD_MAP_WAVES
+#define FSDP_UNSHARD_MAP_WAVES 1
+#endif
+// A fused copy-in whose shard group has one rank writes one destination:
+// it takes the own-slice copy-in's grid.
+#ifndef FSDP_ONE_DEST_OWN
+#define FSDP_ONE_DEST_OWN 1
+#endif
 template <typename F>
 cudaError_t go(F kernel, const KArgs& a, cudaStream_t st, int threads = kThreads, size_t smem = 0,
-               int grid_per_sm = 0, int fallback_per_sm = 0, bool map_waves = false) {
+               int grid_per_sm = 0, int fallback_per_sm = 0, bool map_waves = FSDP_COPY_MAP_WAVES != 0) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     sm_count();
     const int resident = blocks_per_sm(fn, threads, smem);  // also raises the smem limit once
@@ -1485,8 +1523,14 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
         case K_AGIN:
             if (sf && df) return go(ag_copy_in_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
             if (sf) return go(ag_copy_in_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
+            // one destination (the own slice, or a shard group of one rank):
+            // the own-slice policy, many waves over a mapped table too
+            // (2000-parameter pure-TP layer: fused copy-in 0.92 -> 0.965)
+            if (!a.fuse || (FSDP_ONE_DEST_OWN && a.S == 1))
+                return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
+                          FSDP_GRID_OWN, 0, FSDP_OWN_MAP_WAVES != 0);
             return go(ag_copy_in_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
-                      a.fuse ? FSDP_GRID_MULTI : FSDP_GRID_OWN);
+                      FSDP_GRID_MULTI);
         case K_GATHER:
             return sf ? go(ag_gather_kernel<float>, a, st, kThreads, copy_img_bytes<float>())
                       : go(ag_gather_kernel<uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(), FSDP_GRID_GATHER);
@@ -1494,11 +1538,13 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             if (sf && df) return go(ag_unshard_kernel<float, float>, a, st, kThreads, copy_img_bytes<float>());
             if (sf) return go(ag_unshard_kernel<float, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>());
             return go(ag_unshard_kernel<uint16_t, uint16_t>, a, st, kThreads, copy_img_bytes<uint16_t>(),
-                      FSDP_GRID_UNSHARD);
+                      FSDP_GRID_UNSHARD, 0, FSDP_UNSHARD_MAP_WAVES != 0);
         case K_AGOUT:
             return sf ? go(ag_copy_out_kernel<float>, a, st)
                       : go(ag_copy_out_kernel<uint16_t>, a, st, kThreads, 0,
-                           a.shifted ? FSDP_GRID_COPY_SHIFTED : FSDP_GRID_COPY);
+                           a.shifted ? FSDP_GRID_COPY_SHIFTED
+                                     : (a.tile_run ? FSDP_GRID_COPY_MAPPED : FSDP_GRID_COPY),
+                           0, FSDP_AGOUT_MAP_WAVES != 0);
         case K_RSIN:
             return sf ? go(rs_copy_in_kernel<float>, a, st)
                       : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);

@@ -32,6 +32,7 @@ _DT = {"f32": F32, "bf16": BF16, F32: F32, BF16: BF16}
 _OP = {"avg": AVG, "sum": SUM, AVG: AVG, SUM: SUM}
 
 _lib = None
+_threaded = False
 
 
 class OracleError(RuntimeError):
@@ -40,13 +41,21 @@ class OracleError(RuntimeError):
         self.code = code
 
 
+def use_threaded(threaded=True):
+    """Switches this process to the -fopenmp build of the same source (the
+    labelled multi-core CPU baseline; same bytes as the oracle) or back."""
+    global _lib, _threaded
+    if bool(threaded) != _threaded:
+        _lib, _threaded = None, bool(threaded)
+
+
 def lib():
     """Load (building first if needed) the oracle's shared library."""
     global _lib
     if _lib is None:
-        path = _build.library_path()
+        path = _build.library_path(_threaded)
         if not os.path.exists(path):
-            _build.build()
+            _build.build(threaded=_threaded)
         L = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.hor_plan.argtypes = [i32, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]

@@ -18,18 +18,26 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
           "-Wall", "-Wextra", "-Werror"]
 
 
-def library_path():
-    return os.path.join(OUT_DIR, "libhsdp_oracle.so")
+def library_path(threaded: bool = False):
+    return os.path.join(OUT_DIR, "libhsdp_oracle_mt.so" if threaded else "libhsdp_oracle.so")
 
 
-def build(cc: str = "gcc") -> str:
+def build(cc: str = "gcc", threaded: bool = False) -> str:
+    """threaded: a separate build of the same source with -fopenmp, for the
+    labelled multi-core CPU baseline. Its pragmas split only loops whose
+    iterations write disjoint outputs (ranks, parameters, shard rows), so
+    every output element is computed by the same operations in the same
+    order as in the single-threaded build (the oracle). Without -fopenmp
+    the pragmas are ignored."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    out = library_path()
+    out = library_path(threaded)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.run([cc, *CFLAGS, "-I", HERE, SRC, "-o", tmp], check=True)
+    flags = CFLAGS + (["-fopenmp"] if threaded else ["-Wno-unknown-pragmas"])
+    subprocess.run([cc, *flags, "-I", HERE, SRC, "-o", tmp], check=True)
     os.replace(tmp, out)
     return out
 
 
 if __name__ == "__main__":
     print(build())
+    print(build(threaded=True))

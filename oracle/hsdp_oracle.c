@@ -228,6 +228,7 @@ int hor_ag_copy_in(const hor_layout* L, int src_dt, const void* const* shards,
         return HOR_EINVAL;
     if (src_dt == HOR_BF16 && dst_dt == HOR_F32)
         return HOR_EINVAL; /* the cast narrows or keeps, never widens */
+#pragma omp parallel for schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
         int s = w % S;
         int64_t base = (int64_t)s * slice;
@@ -249,6 +250,7 @@ int hor_ag_gather(const hor_layout* L, int dt, int64_t slice, void* const* ag_ou
     int S = L->S, es = elem_bytes(dt);
     if (es == 0)
         return HOR_EINVAL;
+#pragma omp parallel for schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
         int d = w / S;
         for (int sp = 0; sp < S; ++sp) {
@@ -273,6 +275,7 @@ int hor_ag_copy_out(const hor_layout* L, int dt, int64_t slice,
     int P = L->P;
     if (elem_bytes(dt) == 0)
         return HOR_EINVAL;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
         for (int p = 0; p < P; ++p) {
             int64_t dss = L->dss[p], in = L->inner[p];
@@ -299,6 +302,7 @@ int hor_rs_copy_in(const hor_layout* L, int dt, int64_t slice,
     int P = L->P, S = L->S;
     if (elem_bytes(dt) == 0)
         return HOR_EINVAL;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
         for (int sp = 0; sp < S; ++sp) {
             int64_t row = (int64_t)sp * slice;
@@ -342,18 +346,21 @@ int hor_rs_ar_reduce(const hor_layout* L, int dt, int64_t slice_g,
     int S = L->S, D = L->D, W = L->W;
     if (elem_bytes(dt) == 0 || slice_g < slice_f32)
         return HOR_EINVAL;
-    float* vals = (float*)malloc(sizeof(float) * (size_t)(W > 0 ? W : 1));
-    if (!vals)
+    /* one scratch row of W values per rank */
+    float* vals_all = (float*)malloc(sizeof(float) * (size_t)(W > 0 ? W * W : 1));
+    if (!vals_all)
         return HOR_ENOMEM;
+#pragma omp parallel for schedule(dynamic)
     for (int w = 0; w < W; ++w) {
         int s = w % S;
+        float* vals = vals_all + (int64_t)w * W;
         for (int64_t j = 0; j < slice_f32; ++j) {
             for (int v = 0; v < W; ++v)
                 vals[v] = load_as_f32(rs_in[v], dt, (int64_t)s * slice_g + j);
             fused[w][j] = hor_fold_nested(S, D, vals);
         }
     }
-    free(vals);
+    free(vals_all);
     return HOR_OK;
 }
 
@@ -365,6 +372,7 @@ int hor_rs_reduce(const hor_layout* L, int dt, int64_t slice_g, const void* cons
     int S = L->S;
     if (elem_bytes(dt) == 0 || slice_g < slice_f32)
         return HOR_EINVAL;
+#pragma omp parallel for schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
         int d = w / S, s = w % S;
         for (int64_t j = 0; j < slice_f32; ++j) {
@@ -383,6 +391,7 @@ int hor_ar_reduce(const hor_layout* L, int op, int64_t slice_f32, float* const* 
      * all-reduce is scaled by replicate_world_size = D for AVG. In place:
      * every member of the replicate group gets the same result. */
     int S = L->S, D = L->D;
+#pragma omp parallel for schedule(dynamic)
     for (int s = 0; s < S; ++s) {
         for (int64_t j = 0; j < slice_f32; ++j) {
             float total = buf[s][j];
@@ -410,9 +419,10 @@ int hor_apply_grads(const hor_layout* L, const float* const* fused, int op, int 
     if (elem_bytes(dt) == 0)
         return HOR_EINVAL;
     float div = op == HOR_AVG ? (float)L->W : 1.0f;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (int w = 0; w < L->W; ++w) {
-        int s = w % S;
         for (int p = 0; p < P; ++p) {
+            int s = w % S;
             int64_t n = L->len[(int64_t)p * S + s] * L->inner[p];
             void* g = shard_grads[(int64_t)w * P + p];
             for (int64_t k = 0; k < n; ++k) {
