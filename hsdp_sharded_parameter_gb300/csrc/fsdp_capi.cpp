@@ -79,9 +79,12 @@ void build_tables(const fsdp_plan_s& pl, std::vector<Seg> segs[T_COUNT],
         for (int s = 0; s < pl.S; ++s)
             if (sl > 0) segs[T_GATHER_F32 + i].push_back(make_seg(sl, s * sl, s * sl, 0, s));
         tile_prefix(segs[T_GATHER_F32 + i], es, tiles[T_GATHER_F32 + i]);
-        // copy-out: shard s of parameter p goes to rows [off, off+len) of p
-        for (int p = 0; p < pl.P; ++p)
-            for (int s = 0; s < pl.S; ++s) {
+        // copy-out: shard s of parameter p goes to rows [off, off+len) of p.
+        // Listed last parameter first: the copy-in before it in a step
+        // writes the gathered rows in the opposite order, so the copy-out
+        // starts on the rows still in L2 (runs may come in any order).
+        for (int p = pl.P - 1; p >= 0; --p)
+            for (int s = pl.S - 1; s >= 0; --s) {
                 int64_t n = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
                 if (n == 0) continue;
                 segs[T_AGOUT_F32 + i].push_back(
@@ -105,9 +108,12 @@ void build_tables(const fsdp_plan_s& pl, std::vector<Seg> segs[T_COUNT],
             if (sf > 0) segs[T_RS_F32 + i].push_back(make_seg(sf, 0, s * sl, 0, s));
         tile_prefix(segs[T_RS_F32 + i], 4, tiles[T_RS_F32 + i]);
     }
-    // apply: actual shard s of parameter p, from o_p of the fused region
-    for (int s = 0; s < pl.S; ++s)
-        for (int p = 0; p < pl.P; ++p) {
+    // apply: actual shard s of parameter p, from o_p of the fused region.
+    // Listed last shard row and parameter first: the fused reduce before it
+    // writes the fused rows in the opposite order, so the apply starts on
+    // the fused elements still in L2.
+    for (int s = pl.S - 1; s >= 0; --s)
+        for (int p = pl.P - 1; p >= 0; --p) {
             int64_t n = pl.len[(size_t)p * pl.S + s] * pl.inner[p];
             if (n > 0) segs[T_APPLY].push_back(make_seg(n, 0, pl.o[p], p, s));
         }
