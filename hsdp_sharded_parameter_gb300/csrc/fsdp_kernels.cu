@@ -849,6 +849,8 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
     if (st.valid && st.p >= 0 && a.vec) {
         const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(win));
         const int64_t byte0 = (st.src_off + st.rel) * (int64_t)sizeof(S);  // may precede the run: address only
+        bool uniform;
+        unsigned shift;
         if (!same) {
             // one shift for every source? (a per-run constant: steps of a run
             // are whole multiples of 256 elements apart)
@@ -856,27 +858,33 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
             bool ok = true;
             for (int i = lane; i < sh.ns; i += 32)
                 ok = ok && ((reinterpret_cast<uintptr_t>(sp[i]) + (uintptr_t)byte0) & 15u) == sh0;
-            c.uniform = __all_sync(kFull, ok);
-            c.shift = sh0;
-            c.p = st.p;
-            c.row = st.row;
-            c.rep = st.rep;
-            c.dst_off = st.dst_off;
+            uniform = __all_sync(kFull, ok);
+            shift = sh0;
+            if constexpr (slot_cache<RG>()) {
+                c.uniform = uniform;
+                c.shift = sh0;
+                c.p = st.p;
+                c.row = st.row;
+                c.rep = st.rep;
+                c.dst_off = st.dst_off;
+            }
+        } else {
+            uniform = c.uniform;
+            shift = c.shift;
         }
-        if (c.uniform && st.rel >= 0 && st.rel + kStep <= st.n) {
+        if (uniform && st.rel >= 0 && st.rel + kStep <= st.n) {
             // every source window starts `shift` bytes before its first
             // element; a shifted window needs one block more, copied by lane 0
             st.fast = true;
-            st.shift = c.shift;
+            st.shift = shift;
 #pragma unroll
             for (int i = 0; i < sh.ns; ++i) {
-                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0 - c.shift + lane * 16;
-                const uint32_t s0 = sbase + (uint32_t)((i * kWin + lane) * 16);
+                const char* g = reinterpret_cast<const char*>(sp[i]) + byte0 - shift;
 #pragma unroll
-                for (int v = 0; v < RG * Raw<S>::kVec; ++v) cp_async16(s0 + (uint32_t)(v * 32 * 16), g + v * 32 * 16);
-                if (c.shift != 0 && lane == 0)
-                    cp_async16(sbase + (uint32_t)((i * kWin + kWin - 1) * 16),
-                               reinterpret_cast<const char*>(sp[i]) + byte0 - c.shift + (kWin - 1) * 16);
+                for (int v = 0; v < RG * Raw<S>::kVec; ++v)
+                    cp_async16(sbase + (uint32_t)((i * kWin + lane + 32 * v) * 16), g + (lane + 32 * v) * 16);
+                if (shift != 0 && lane == 0)
+                    cp_async16(sbase + (uint32_t)((i * kWin + kWin - 1) * 16), g + (kWin - 1) * 16);
             }
         } else {
             const int64_t e_lo = st.rel < 0 ? 0 : st.rel;
@@ -893,7 +901,7 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
                 }
             }
         }
-    } else if (st.valid && !same) {
+    } else if (slot_cache<RG>() && st.valid && !same) {
         // zero runs and unaligned destinations stage no windows; the slot
         // now holds this run's pointers
         c.p = st.p;
