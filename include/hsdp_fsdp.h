@@ -143,12 +143,13 @@ int fsdp_plan_upload(fsdp_plan_t plan);
 
 /* Caps the number of thread blocks every later data call of this plan
  * launches (0, the default: each kernel's own grid, many short waves of
- * blocks on long launches). The
- * kernels stride over their work, so any cap gives the same results; a
- * small cap leaves the other SMs to kernels running beside them, e.g. the
- * backward compute the gradient sync overlaps with, the way the pages'
- * communication streams run beside compute [OVERLAP §二.2]. May be changed
- * between calls. */
+ * blocks on long launches). The kernels stride over their work, so any cap
+ * gives the same results; a small cap leaves the other SMs to kernels
+ * running beside them, e.g. the backward compute the gradient sync overlaps
+ * with, the way the pages' communication streams run beside compute
+ * [OVERLAP §二.2]. Under a cap the reductions (fused RS+AR, ReduceScatter,
+ * AllReduce) run one block per SM with up to 16 warps, so max_blocks is
+ * the number of SMs they occupy. May be changed between calls. */
 int fsdp_plan_set_grid_limit(fsdp_plan_t plan, int max_blocks);
 
 /* Diagnostic, with no counterpart in the pages: builds the plan's work
