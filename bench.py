@@ -59,6 +59,11 @@ def parse(argv=None):
                     help="scale every dim 0 (small cases for profiler captures only)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step replayed from a CUDA graph (launch-bound workloads)")
+    ap.add_argument("--profile-kernel", default=None,
+                    choices=["ag_copy_in", "ag_copy_out", "rs_ar_reduce", "apply_grads", "ag_unshard"],
+                    help="the small case of an ncu capture: only this kernel, --launches times, on the "
+                         "workload scaled by --scale with only its buffers allocated (prints no bench line)")
+    ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--pipeline", type=int, default=0, metavar="LAYERS",
                     help="also measure the pipelined backward over LAYERS layers of the workload")
     return ap.parse_args(argv)
@@ -789,6 +794,71 @@ def run_e2e(args, unit, calls, step_bytes, world, dev):
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 2), "steps": args.e2e_steps}
 
 
+def run_profile_case(args, wl):
+    """One kernel of the step, args.launches times, on the workload with
+    every dim 0 scaled by args.scale and only the buffers that kernel reads
+    and writes allocated: the case an ncu capture of that kernel runs."""
+    import torch
+
+    from hsdp_sharded_parameter_gb300 import capi as C
+    from hsdp_sharded_parameter_gb300 import workloads as WL
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    d0 = wl.d0 if args.scale == 1.0 else scaled_workload(wl, args.scale)[0]
+    plan = C.Plan(d0, wl.inner, wl.rank_size, wl.shard_size).upload()
+    W, S, P = plan.W, plan.S, plan.P
+    pdt, gdt = wl.param_dtype, wl.grad_dtype
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+    def alloc(sizes, dt):
+        return [torch.empty(int(n), dtype=tdt[dt], device=dev) for n in sizes]
+
+    shard_sizes = [plan.shard_numel(p, w % S) for w in range(W) for p in range(P)]
+    full_sizes = [plan.numel(p) for _ in range(W) for p in range(P)]
+    k = args.profile_kernel
+    if k in ("ag_copy_in", "ag_unshard"):
+        src = alloc(shard_sizes, pdt)
+        WL.torch_fill_(src, wl.seed_params, wl.param_std, pdt)
+        b_src = plan.bind("shards", pdt, src)
+    if k == "ag_copy_in":
+        dst = alloc([S * plan.slice_numel(pdt)] * W, pdt)
+        b_dst = plan.bind("ag_output", pdt, dst)
+        call = lambda: C.fsdp_ag_copy_in(plan, b_src, b_dst, True)  # noqa: E731
+    elif k == "ag_unshard":
+        dst = alloc(full_sizes, pdt)
+        b_dst = plan.bind("full_params", pdt, dst)
+        call = lambda: C.fsdp_ag_unshard(plan, b_src, b_dst)  # noqa: E731
+    elif k == "ag_copy_out":
+        src = alloc([S * plan.slice_numel(pdt)] * W, pdt)
+        WL.torch_fill_(src, wl.seed_params, wl.param_std, pdt)
+        dst = alloc(full_sizes, pdt)
+        b_src, b_dst = plan.bind("ag_output", pdt, src), plan.bind("full_params", pdt, dst)
+        call = lambda: C.fsdp_ag_copy_out(plan, b_src, b_dst)  # noqa: E731
+    elif k == "rs_ar_reduce":
+        src = alloc(full_sizes, gdt)
+        WL.torch_fill_(src, wl.seed_grads, wl.grad_std, gdt)
+        dst = alloc([plan.slice_numel("f32")] * W, "f32")
+        b_src, b_dst = plan.bind("grads", gdt, src), plan.bind("fused", "f32", dst)
+        call = lambda: C.fsdp_rs_ar_reduce(plan, b_src, b_dst)  # noqa: E731
+    else:
+        src = alloc([plan.slice_numel("f32")] * W, "f32")
+        WL.torch_fill_(src, wl.seed_grads, wl.grad_std, "f32")
+        dst = alloc(shard_sizes, gdt)
+        b_src, b_dst = plan.bind("fused", "f32", src), plan.bind("shard_grads", gdt, dst)
+        call = lambda: C.fsdp_apply_grads(plan, b_src, "avg", b_dst)  # noqa: E731
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for i in range(args.launches):
+        ev[0].record()
+        call()
+        ev[1].record()
+        torch.cuda.synchronize()
+        print(f"{k} {wl.key} dim0 x{args.scale:g} launch {i}: {ev[0].elapsed_time(ev[1]) * 1e3:.1f} us",
+              flush=True)
+    print(f"{k}: {sum(t.numel() * t.element_size() for t in src + dst) / 1e9:.2f} GB on the device", flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse(argv)
     from hsdp_sharded_parameter_gb300 import workloads as WL
@@ -796,6 +866,8 @@ def main(argv=None):
     wl = WL.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.profile_kernel:
+        return run_profile_case(args, wl)
     return run_gpu(args, wl)
 
 

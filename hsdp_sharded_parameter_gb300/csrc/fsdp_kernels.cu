@@ -1204,24 +1204,16 @@ __device__ __forceinline__ void direct_reduce_body(const KArgs& a) {
 // ----------------------------------------------------------- entry kernels
 // One named kernel per C-ABI call (the names show in profiles).
 
-// Minimum resident blocks per SM the copy and apply kernels are compiled
-// for (caps their registers: 2 -> 128, 3 -> 85 per thread).
-#ifndef FSDP_COPY_MINB
-#define FSDP_COPY_MINB 1
-#endif
-#ifndef FSDP_APPLY_MINB
-#define FSDP_APPLY_MINB 1
-#endif
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D, true>(a); }
+__global__ void __launch_bounds__(kThreads) ag_copy_in_kernel(const KArgs a) { copy_body<K_AGIN, S, D, true>(a); }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ag_gather_kernel(const KArgs a) { copy_body<K_GATHER, T, T, true>(a); }
 template <typename T>
-__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
+__global__ void __launch_bounds__(kThreads) ag_copy_out_kernel(const KArgs a) { copy_body<K_AGOUT, T, T, false>(a); }
 template <typename T>
 __global__ void __launch_bounds__(kThreads) rs_copy_in_kernel(const KArgs a) { copy_body<K_RSIN, T, T, false>(a); }
 template <typename S, typename D>
-__global__ void __launch_bounds__(kThreads, FSDP_COPY_MINB) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
+__global__ void __launch_bounds__(kThreads) ag_unshard_kernel(const KArgs a) { copy_body<K_UNSHARD, S, D, true>(a); }
 // The unfused ReduceScatter over a shard group of one rank: a widening copy
 // (the sum of one term, divided by 1).
 template <typename S>
@@ -1289,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads) ar_reduce_wide_kernel(const KArgs a)
     direct_reduce_body<K_AR, float>(a);
 }
 template <typename D>
-__global__ void __launch_bounds__(kThreads, FSDP_APPLY_MINB) apply_grads_kernel(const KArgs a) { apply_body<D>(a); }
+__global__ void __launch_bounds__(kThreads) apply_grads_kernel(const KArgs a) { apply_body<D>(a); }
 
 // ------------------------------------------------------------------ launch
 
