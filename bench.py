@@ -516,6 +516,13 @@ def run_gpu(args, wl):
     ub = sizes["shard_total"] * ES[wl.param_dtype] + sizes["W"] * sizes["N"] * ES[wl.param_dtype]
     extra["ag_unshard"] = entry(per_launch_us(unit.unshard_direct), ub)
     extra["ag_unshard"]["replaces_us"] = round(kernels["ag_copy_in"]["us"] + kernels["ag_copy_out"]["us"], 2)
+    # the gradient sync in one pass (fused reduce with the apply folded in):
+    # reads every gradient once, writes the fused regions and the shard
+    # gradients; the apply's read of the fused regions is gone
+    ob = sizes["W"] * sizes["N"] * ES[wl.grad_dtype] + sizes["W"] * sizes["slice_f32"] * 4 \
+        + sizes["shard_total"] * ES[wl.grad_dtype]
+    extra["rs_ar_reduce_apply"] = entry(per_launch_us(lambda: unit.reduce_grads_one_pass("avg")), ob)
+    extra["rs_ar_reduce_apply"]["replaces_us"] = round(kernels["rs_ar_reduce"]["us"] + kernels["apply_grads"]["us"], 2)
     ubytes = unfused_bytes(sizes, wl.param_dtype, wl.param_dtype, wl.grad_dtype)
     unfused_calls = {
         "ag_copy_in_own_slice": lambda: unit.ag_copy_in(fuse_gather=False),
@@ -650,11 +657,28 @@ def run_per_workload(args, dev, peak):
             gbs = kb[n] / (us * 1e-6) / 1e9
             kernels[n] = {"us": round(us, 2), "bytes": kb[n], "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
         step_us = sum(ev[k][0].elapsed_time(ev[k][len(calls)]) for k in range(K)) / K * 1e3
+        # the gradient sync in one pass (outside the step), back to back
+        ob = sizes["W"] * sizes["N"] * ES[wl.grad_dtype] + sizes["W"] * sizes["slice_f32"] * 4 \
+            + sizes["shard_total"] * ES[wl.grad_dtype]
+        for _ in range(3):
+            unit.reduce_grads_one_pass("avg")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            if flush:
+                scratch.zero_()
+            unit.reduce_grads_one_pass("avg")
+        e1.record(stream)
+        torch.cuda.synchronize()
+        one_us = e0.elapsed_time(e1) / K * 1e3
+        one = {"us": round(one_us, 2), "bytes": ob, "gbs": round(ob / (one_us * 1e-6) / 1e9, 1),
+               "frac": round(ob / (one_us * 1e-6) / 1e9 / peak, 4),
+               "replaces_us": round(kernels["rs_ar_reduce"]["us"] + kernels["apply_grads"]["us"], 2)}
         out[key] = {"rank_size": wl.rank_size, "shard_size": wl.shard_size, "params": wl.n_params,
                     "elements_per_rank": sizes["N"], "steps": K, "step_us": round(step_us, 2),
                     "step_bytes": step_bytes, "step_gbs": round(step_bytes / (step_us * 1e-6) / 1e9, 1),
                     "l2": "flushed between steps" if flush else "working set larger than L2",
-                    "kernels": kernels}
+                    "kernels": kernels, "rs_ar_reduce_apply": one}
         unit.close()
         plan.close()
         del unit, scratch

@@ -85,6 +85,7 @@ def lib():
         L.fsdp_rs_ar_reduce.argtypes = [vp, vp, vp, vp]
         L.fsdp_apply_grads.argtypes = [vp, vp, i32, i32, vp, vp]
         L.fsdp_rs_reduce.argtypes = [vp, vp, i32, vp, vp]
+        L.fsdp_rs_ar_reduce_apply.argtypes = [vp, vp, vp, i32, i32, vp, vp]
         L.fsdp_ar_reduce.argtypes = [vp, vp, i32, vp]
         L.fsdp_rs_ar_reduce_noalloc.argtypes = [vp, i32, vp, vp, vp]
         L.fsdp_ag_unshard.argtypes = [vp, vp, vp, vp]
@@ -291,6 +292,11 @@ def fsdp_rs_ar_reduce(plan, grads, fused, stream=None):
 def fsdp_apply_grads(plan, fused, op, shard_grads, accumulate=False, stream=None):
     _check(lib().fsdp_apply_grads(plan.handle, fused.handle, OPS.get(op, op), int(bool(accumulate)),
                                   shard_grads.handle, _stream(stream)))
+
+
+def fsdp_rs_ar_reduce_apply(plan, grads, fused, op, shard_grads, accumulate=False, stream=None):
+    _check(lib().fsdp_rs_ar_reduce_apply(plan.handle, grads.handle, fused.handle, OPS.get(op, op),
+                                         int(bool(accumulate)), shard_grads.handle, _stream(stream)))
 
 
 def fsdp_rs_reduce(plan, rs_in, op, fused, stream=None):

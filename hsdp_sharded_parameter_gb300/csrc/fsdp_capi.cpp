@@ -775,6 +775,35 @@ int fsdp_apply_grads(fsdp_plan_t pl, fsdp_binding_t fused, int op, int accumulat
     return run(K_APPLY, FSDP_F32, shard_grads->dt, a, stream, "apply_grads");
 }
 
+int fsdp_rs_ar_reduce_apply(fsdp_plan_t pl, fsdp_binding_t grads, fsdp_binding_t fused, int op, int accumulate,
+                            fsdp_binding_t shard_grads, fsdp_stream_t stream) {
+    clear_error();
+    int rc;
+    if ((rc = check_ready(pl, "rs_ar_reduce_apply"))) return rc;
+    if ((rc = check_binding(pl, grads, FSDP_ROLE_GRADS, "rs_ar_reduce_apply"))) return rc;
+    if ((rc = check_binding(pl, fused, FSDP_ROLE_FUSED, "rs_ar_reduce_apply"))) return rc;
+    if ((rc = check_binding(pl, shard_grads, FSDP_ROLE_SHARD_GRADS, "rs_ar_reduce_apply"))) return rc;
+    if (op != FSDP_AVG && op != FSDP_SUM) return set_error(FSDP_ERR_INVALID_ARG, "rs_ar_reduce_apply: unknown op");
+    if (shard_grads->dt != grads->dt)
+        return set_error(FSDP_ERR_INVALID_ARG, "rs_ar_reduce_apply: shard gradients must have the gradient dtype");
+    if (!can_fold_apply(grads->dt, pl->W, pl->D)) {
+        // too many sources for the staged reduce: the two calls it stands for
+        if ((rc = fsdp_rs_ar_reduce(pl, grads, fused, stream))) return rc;
+        return fsdp_apply_grads(pl, fused, op, accumulate, shard_grads, stream);
+    }
+    KArgs a = base_args(pl, T_RSAR, 1);
+    a.src_tab = grads->dev_table;
+    a.dst_tab = fused->dev_table;
+    a.sg_tab = shard_grads->dev_table;
+    a.vec = fused->aligned16;
+    a.op = op;
+    a.accumulate = accumulate ? 1 : 0;
+    // the fused buffer keeps the raw sum; the shard gradients divide by W
+    // for AVG, as fsdp_apply_grads does [OVERLAP PR #758 §二.3]
+    set_divisor(a, op == FSDP_AVG ? pl->W : 1);
+    return run(K_RSAR, grads->dt, FSDP_F32, a, stream, "rs_ar_reduce_apply");
+}
+
 int fsdp_rs_reduce(fsdp_plan_t pl, fsdp_binding_t rs_in, int op, fsdp_binding_t fused, fsdp_stream_t stream) {
     clear_error();
     int rc;

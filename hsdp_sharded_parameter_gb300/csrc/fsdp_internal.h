@@ -104,6 +104,9 @@ struct KArgs {
     // the destination's 16-byte grid (copy-out picks its grid by it).
     int shifted;
     int dests;  // destinations written per tile when more than one (the gather)
+    // The fused reduce with the apply folded in: the [W][P] table of
+    // actual-shard gradients it also writes (nullptr: not folded in).
+    void* const* sg_tab;
 };
 
 // Fills div, scale_mode and recip for a divisor d >= 1.
@@ -128,6 +131,10 @@ enum Kind {
 // Launches the kernel of `kind` for the given element types. Returns a
 // cudaError_t of the launch.
 cudaError_t launch(Kind kind, int src_dt, int dst_dt, const KArgs& a, cudaStream_t stream);
+
+// Whether the fused reduce of W sources (D replicas) of this dtype can fold
+// the apply in (its staged form fits with the replicas' gradient pointers).
+bool can_fold_apply(int src_dt, int W, int D);
 
 }  // namespace fsdp
 

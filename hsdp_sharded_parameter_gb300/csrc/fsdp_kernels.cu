@@ -829,7 +829,7 @@ struct Shape {
 // aligned copies exactly the RG * 256 elements of each source, RG blocks per
 // lane per 16-byte vector. Always commits one group (possibly empty) so the
 // group count stays in step with the ring.
-template <int KIND, typename S, int NS, int SIN, int ND, int RG>
+template <int KIND, typename S, int NS, int SIN, int ND, int RG, bool AP = false>
 __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage, SlotCache& c,
                                            const Shape<KIND, NS, SIN, ND>& sh) {
     const int lane = threadIdx.x & 31;
@@ -844,6 +844,13 @@ __device__ __forceinline__ void stage_step(const KArgs& a, Step& st, char* stage
         if (st.p >= 0)
             for (int i = lane; i < sh.ns; i += 32) sp[i] = ReduceShape<KIND>::template src<S>(a, st.p, st.row, st.rep, i);
         for (int j = lane; j < sh.nd; j += 32) dp[j] = ReduceShape<KIND>::dst(a, st.row, st.rep, j) + st.dst_off;
+        if constexpr (AP) {
+            // replica j's actual-shard gradient of this run's parameter
+            S** gp = reinterpret_cast<S**>(stage + Staging<S, RG>::window_bytes(sh.ns) + (sh.ns + sh.nd) * sizeof(void*));
+            if (st.p >= 0)
+                for (int j = lane; j < sh.nd; j += 32)
+                    gp[j] = static_cast<S*>(a.sg_tab[(int64_t)(j * a.S + st.row) * a.P + st.p]);
+        }
     }
     __syncwarp();
     if (st.valid && st.p >= 0 && a.vec) {
@@ -979,7 +986,37 @@ __device__ __forceinline__ void fold_fast(const uint4* win, int lane, int g, uns
     }
 }
 
-template <int KIND, typename S, int NS, int SIN, int ND, int RG>
+// The apply folded into the fused reduce: the 8 fused sums of a granule,
+// divided as KArgs says (W for AVG), added to the gradient already there
+// when accumulating, rounded once to the gradient dtype and stored at g,
+// the granule's first actual-shard element of one replica. The same
+// operations in the same order as the apply kernel; g may sit at any
+// element alignment (16-, 8- or 2/4-byte stores).
+template <typename G>
+__device__ __forceinline__ void store_applied(const KArgs& a, const float (&sum)[8], G* g) {
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = a.div != 1.0f ? scaled(sum[e], a) : sum[e];
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(g);
+    if (a.accumulate) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(load_f32(g, e), x[e]);
+    }
+    Raw<G> r;
+    narrow(x, r);
+    if ((addr & 15u) == 0) {
+        store_raw(g, r);
+    } else if ((addr & 7u) == 0) {
+        uint2* q = reinterpret_cast<uint2*>(g);
+#pragma unroll
+        for (int v = 0; v < Raw<G>::kWords / 2; ++v) q[v] = make_uint2(r.w[2 * v], r.w[2 * v + 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) store_f32(g, e, x[e]);
+    }
+}
+
+template <int KIND, typename S, int NS, int SIN, int ND, int RG, bool AP = false>
 __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, const char* stage,
                                              const Shape<KIND, NS, SIN, ND>& sh, uint4* img, int& parity) {
     if (!st.valid) return;
@@ -988,8 +1025,13 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
     const S* const* sp = reinterpret_cast<const S* const*>(stage + Staging<S, RG>::window_bytes(sh.ns));
     float* const* dp =
         reinterpret_cast<float* const*>(stage + Staging<S, RG>::window_bytes(sh.ns) + sh.ns * sizeof(void*));
+    // with the apply folded in: the replicas' actual-shard gradients
+    S* const* gp = reinterpret_cast<S* const*>(stage + Staging<S, RG>::window_bytes(sh.ns) +
+                                               (sh.ns + sh.nd) * sizeof(void*));
     constexpr size_t kImg = fan_img_bytes<RG>();
-    const bool scale = a.div != 1.0f;
+    // the fused region holds the raw sum; with the apply folded in, a.div
+    // is the apply's divisor
+    const bool scale = !AP && a.div != 1.0f;
     if (st.fast) {
         Raw<float> o[RG];
 #pragma unroll
@@ -1002,6 +1044,10 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
             if (scale) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
+            }
+            if constexpr (AP) {
+#pragma unroll
+                for (int j = 0; j < sh.nd; ++j) store_applied(a, total, gp[j] + st.rel + g * kStepElems + lane * kGran);
             }
             narrow(total, o[g]);
         }
@@ -1074,6 +1120,9 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
 #pragma unroll
                     for (int e = 0; e < 8; ++e) total[e] = scaled(total[e], a);
                 }
+                if constexpr (AP) {
+                    for (int j = 0; j < sh.nd; ++j) store_applied(a, total, gp[j] + rel);
+                }
             }
             Raw<float> o;
             narrow(total, o);
@@ -1086,6 +1135,14 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
                 if (st.p >= 0) {
                     v = fold_elem<KIND, S>(a, sp, st.src_off + e);
                     if (scale) v = scaled(v, a);
+                    if constexpr (AP) {
+                        float q = a.div != 1.0f ? scaled(v, a) : v;
+                        for (int j = 0; j < sh.nd; ++j) {
+                            float x = q;
+                            if (a.accumulate) x = __fadd_rn(load_f32(gp[j], e), x);
+                            store_f32(gp[j], e, x);
+                        }
+                    }
                 }
                 for (int j = 0; j < sh.nd; ++j) dp[j][e] = v;
             }
@@ -1096,11 +1153,13 @@ __device__ __forceinline__ void consume_step(const KArgs& a, const Step& st, con
 // Two-stage ring per warp: while step i is folded from shared memory, the
 // copies of step i+1 are in flight. Each lane waits for its own copies;
 // __syncwarp then makes every lane's copies visible to the whole warp.
-template <int KIND, typename S, int NS, int SIN, int ND, int RG = 1>
+template <int KIND, typename S, int NS, int SIN, int ND, int RG = 1, bool AP = false>
 __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
     extern __shared__ __align__(16) char smem_raw[];
     const Shape<KIND, NS, SIN, ND> sh(a);
-    const size_t sb = Staging<S, RG>::stage_bytes(sh.ns, sh.nd);
+    // with the apply folded in, each stage also holds the replicas'
+    // shard-gradient pointers
+    const size_t sb = Staging<S, RG>::stage_bytes(sh.ns, AP ? 2 * sh.nd : sh.nd);
     constexpr bool kFan = fan_out<KIND, NS, ND>();
     char* base = smem_raw + (threadIdx.x >> 5) * (2 * sb + (kFan ? 2 * fan_img_bytes<RG>() : 0));
     char* here = base;        // stage of the step being folded
@@ -1111,13 +1170,13 @@ __device__ __forceinline__ void staged_reduce_body(const KArgs& a) {
     StepGen<RG> gen;
     gen.init(a);
     Step cur = gen.next(a);
-    stage_step<KIND, S, NS, SIN, ND, RG>(a, cur, here, c_here, sh);
+    stage_step<KIND, S, NS, SIN, ND, RG, AP>(a, cur, here, c_here, sh);
     while (cur.valid) {
         Step nxt = gen.next(a);
-        stage_step<KIND, S, NS, SIN, ND, RG>(a, nxt, there, c_there, sh);
+        stage_step<KIND, S, NS, SIN, ND, RG, AP>(a, nxt, there, c_there, sh);
         cp_async_wait1();
         __syncwarp();
-        consume_step<KIND, S, NS, SIN, ND, RG>(a, cur, here, sh, img, parity);
+        consume_step<KIND, S, NS, SIN, ND, RG, AP>(a, cur, here, sh, img, parity);
         __syncwarp();
         cur = nxt;
         char* t = here;
@@ -1221,6 +1280,11 @@ __global__ void __launch_bounds__(kThreads) rs_reduce_copy_kernel(const KArgs a)
 template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_ar_reduce_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND>(a);
+}
+// The fused reduce with the apply folded in (fsdp_rs_ar_reduce_apply).
+template <typename S, int NS, int SIN, int ND>
+__global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm) rs_ar_reduce_apply_kernel(const KArgs a) {
+    staged_reduce_body<K_RSAR, S, NS, SIN, ND, 1, true>(a);
 }
 template <typename S, int NS>
 __global__ void __launch_bounds__(kStagedWarps * 32, kStagedBlocksPerSm)rs_reduce_kernel(const KArgs a) {
@@ -1549,6 +1613,25 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return sf ? go(rs_copy_in_kernel<float>, a, st)
                       : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);
         case K_RSAR:
+            if (a.sg_tab) {
+                // the apply folded in (can_fold_apply said the shape fits);
+                // each stage holds 2 * D destination pointers
+                if (sf) {
+                    if (a.W == 4 && a.S == 4)
+                        return go_staged<float>(rs_ar_reduce_apply_kernel<float, 4, 4, 1>, a, st, 4, 2, false,
+                                                rsar_grid(false));
+                    return go_staged<float>(rs_ar_reduce_apply_kernel<float, 0, 0, 0>, a, st, a.W, 2 * a.D, false,
+                                            rsar_grid(false));
+                }
+#define FSDP_RSAR_AP(W_, S_)                                                                                \
+    if (a.W == W_ && a.S == S_)                                                                             \
+        return go_staged<uint16_t>(rs_ar_reduce_apply_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, 2 * (W_ / S_), \
+                                   fan_out<K_RSAR, W_, W_ / S_>(), rsar_grid(fan_out<K_RSAR, W_, W_ / S_>()));
+                FSDP_RSAR_AP(16, 8) FSDP_RSAR_AP(8, 4) FSDP_RSAR_AP(8, 8) FSDP_RSAR_AP(8, 1) FSDP_RSAR_AP(4, 4)
+#undef FSDP_RSAR_AP
+                return go_staged<uint16_t>(rs_ar_reduce_apply_kernel<uint16_t, 0, 0, 0>, a, st, a.W, 2 * a.D, false,
+                                           rsar_grid(false));
+            }
             if (a.max_grid > 0 && (sf ? staged_fits<float>(a.W, a.D) : staged_fits<uint16_t>(a.W, a.D))) {
                 if (sf) {
                     if (a.W == 4 && a.S == 4)
@@ -1629,6 +1712,10 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
                       : go(apply_grads_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_APPLY);
     }
     return cudaErrorInvalidValue;
+}
+
+bool can_fold_apply(int src_dt, int W, int D) {
+    return src_dt == FSDP_F32 ? staged_fits<float>(W, 2 * D) : staged_fits<uint16_t>(W, 2 * D);
 }
 
 }  // namespace fsdp

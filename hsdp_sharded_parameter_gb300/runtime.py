@@ -89,6 +89,12 @@ class HsdpUnit:
         self.rs_ar_reduce(stream)
         self.apply_grads(op, accumulate, stream)
 
+    def reduce_grads_one_pass(self, op="avg", accumulate=False, stream=None):
+        """reduce_grads with the apply folded into the fused reduce (the same
+        bits in the fused buffer and the shard gradients, one pass)."""
+        C.fsdp_rs_ar_reduce_apply(self.plan, self.b_grads, self.b_fused, op, self.b_shard_grads, accumulate,
+                                  stream)
+
     def reduce_grads_unfused(self, op="avg", stream=None):
         assert self.rs_in is not None, "built without the unfused path"
         C.fsdp_rs_copy_in(self.plan, self.b_grads, self.b_rs_in, stream)

@@ -287,6 +287,19 @@ int fsdp_rs_reduce(fsdp_plan_t plan, fsdp_binding_t rs_in, int op, fsdp_binding_
  * apply_grads (AVG) bit for bit. */
 int fsdp_ar_reduce(fsdp_plan_t plan, fsdp_binding_t fused, int op, fsdp_stream_t stream);
 
+/* fsdp_rs_ar_reduce followed by fsdp_apply_grads, in one pass: the fused
+ * regions get exactly the bits fsdp_rs_ar_reduce writes (the raw SUM) and
+ * the actual-shard gradients exactly the bits fsdp_apply_grads would write
+ * from them (op, accumulate as there), without reading the fused regions
+ * back: the apply's divide, back-fill of the actual rows and rounding
+ * ([OVERLAP] PR #758 §二.3, [RAGGED] §6.4) happen where the sum is formed.
+ * No counterpart as one call in the pages (which apply after the fused
+ * AllReduce). shard_grads must have the gradient dtype. One kernel when the
+ * staged reduce fits the mesh (up to 32 bf16 or ~26 fp32 sources);
+ * otherwise the two calls it stands for, in order on `stream`. */
+int fsdp_rs_ar_reduce_apply(fsdp_plan_t plan, fsdp_binding_t grads, fsdp_binding_t fused, int op,
+                            int accumulate, fsdp_binding_t shard_grads, fsdp_stream_t stream);
+
 /* ------------------------------------------------ allocation-free call */
 
 /* Size of the fixed device work area of fsdp_rs_ar_reduce_noalloc. */

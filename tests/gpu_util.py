@@ -185,6 +185,28 @@ def check_every_step(L, unit, alloc, seed=0, special=False, ops=("avg", "sum")):
         assert cmp(to_np(g), r, gdt), "apply_grads accumulate"
         n += 1
 
+    # backward in one pass: the fused reduce with the apply folded in (the
+    # same fused regions and shard gradients), fresh and accumulating
+    for op in ops:
+        dirty(unit.fused)
+        dirty(unit.shard_grads)
+        unit.reduce_grads_one_pass(op)
+        ref = O.apply_grads(L, ref_fused, op, gdt)
+        torch.cuda.synchronize()
+        for g, r in zip(unit.fused, ref_fused):
+            assert cmp(to_np(g), r, "f32"), f"rs_ar_reduce_apply fused {op}"
+            n += 1
+        for g, r in zip(unit.shard_grads, ref):
+            assert cmp(to_np(g), r, gdt), f"rs_ar_reduce_apply shard grads {op}"
+            n += 1
+    before = [to_np(t) for t in unit.shard_grads]
+    unit.reduce_grads_one_pass("sum", accumulate=True)
+    ref = O.apply_grads(L, ref_fused, "sum", gdt, accumulate=True, shard_grads=[b.copy() for b in before])
+    torch.cuda.synchronize()
+    for g, r in zip(unit.shard_grads, ref):
+        assert cmp(to_np(g), r, gdt), "rs_ar_reduce_apply accumulate"
+        n += 1
+
     # backward, unfused: RS copy-in, RS, AR, apply
     dirty(unit.rs_in)
     C.fsdp_rs_copy_in(unit.plan, unit.b_grads, unit.b_rs_in)

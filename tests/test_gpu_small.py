@@ -128,6 +128,16 @@ def test_each_call_launches_exactly_one_kernel():
     unit.reduce_grads_unfused()
     torch.cuda.synchronize()
     assert C.fsdp_launch_count() - c0 == 7
+    c0 = C.fsdp_launch_count()
+    unit.reduce_grads_one_pass()  # the fused reduce with the apply folded in
+    torch.cuda.synchronize()
+    assert C.fsdp_launch_count() - c0 == 1
+    # a mesh too wide for the staged reduce: the two calls it stands for
+    plan, L, unit, alloc = make(8, 5, [7, 16], [8, 1], "bf16", "bf16")
+    c0 = C.fsdp_launch_count()
+    unit.reduce_grads_one_pass()
+    torch.cuda.synchronize()
+    assert C.fsdp_launch_count() - c0 == 2
 
 
 def test_empty_and_degenerate_plans():

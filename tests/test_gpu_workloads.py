@@ -67,6 +67,17 @@ def test_direct_unshard_full_size(key):
     free(unit, plan)
 
 
+@pytest.mark.parametrize("key", ["hsdp_2x4_llama", "ragged_fsdp", "pure_tp_compat", "large_hsdp"])
+def test_one_pass_sync_full_size(key):
+    # the fused reduce with the apply folded in gives the oracle's fused
+    # regions and shard gradients, every byte
+    wl, plan, L, unit = build(key)
+    unit.reduce_grads_one_pass("avg")
+    torch.cuda.synchronize()
+    FP.check_unit(L, unit, "avg", forward=False)
+    free(unit, plan)
+
+
 def test_pure_tp_sum_op():
     # the DTensor-managed (pure TP) default is SUM ("Hyper通信掩盖方案" PR #758 §二.3)
     wl, plan, L, unit = build("pure_tp_compat")
