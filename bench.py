@@ -60,7 +60,8 @@ def parse(argv=None):
     ap.add_argument("--graph", action="store_true",
                     help="also time the step replayed from a CUDA graph (launch-bound workloads)")
     ap.add_argument("--profile-kernel", default=None,
-                    choices=["ag_copy_in", "ag_copy_out", "rs_ar_reduce", "apply_grads", "ag_unshard"],
+                    choices=["ag_copy_in", "ag_copy_out", "rs_ar_reduce", "apply_grads", "ag_unshard",
+                             "rs_ar_reduce_apply"],
                     help="the small case of an ncu capture: only this kernel, --launches times, on the "
                          "workload scaled by --scale with only its buffers allocated (prints no bench line)")
     ap.add_argument("--launches", type=int, default=3)
@@ -731,19 +732,22 @@ def run_pipeline(args, wl, d0, dev):
     out = {"layers": n, "workload": wl.key, "gemms_per_layer": k, "gemm": "8192^3 bf16"}
     t_comp = timed(lambda: [compute(L) for L in reversed(range(n))])
     out["compute_only_ms"] = round(t_comp, 3)
-    for fused in (True, False):
-        name = "fused" if fused else "unfused_4step"
-        if fused:
+    for mode in ("fused", "one_pass", "unfused"):
+        fused, one = mode != "unfused", mode == "one_pass"
+        name = {"fused": "fused", "one_pass": "fused_one_pass", "unfused": "unfused_4step"}[mode]
+        if one:
+            t_sync = timed(lambda: [units[L].reduce_grads_one_pass("avg") for L in reversed(range(n))])
+        elif fused:
             t_sync = timed(lambda: [units[L].reduce_grads("avg") for L in reversed(range(n))])
         else:
             t_sync = timed(lambda: [units[L].reduce_grads_unfused("avg") for L in reversed(range(n))])
         res = {"sync_only_ms": round(t_sync, 3), "serial_ms": round(t_comp + t_sync, 3)}
         # sync kernels on the whole GPU (0) or on a capped number of blocks
         for cap in (0, 64, 96, 112, 128):
-            t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap).run(compute))
+            t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap, one_pass=one).run(compute))
             hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
             res[f"comm_blocks_{cap}"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
-        t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, sync_priority=0).run(compute))
+        t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, sync_priority=0, one_pass=one).run(compute))
         hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
         res["sync_low_priority"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
         out[name] = res
@@ -859,12 +863,17 @@ def run_profile_case(args, wl):
         dst = alloc(full_sizes, pdt)
         b_src, b_dst = plan.bind("ag_output", pdt, src), plan.bind("full_params", pdt, dst)
         call = lambda: C.fsdp_ag_copy_out(plan, b_src, b_dst)  # noqa: E731
-    elif k == "rs_ar_reduce":
+    elif k in ("rs_ar_reduce", "rs_ar_reduce_apply"):
         src = alloc(full_sizes, gdt)
         WL.torch_fill_(src, wl.seed_grads, wl.grad_std, gdt)
         dst = alloc([plan.slice_numel("f32")] * W, "f32")
         b_src, b_dst = plan.bind("grads", gdt, src), plan.bind("fused", "f32", dst)
         call = lambda: C.fsdp_rs_ar_reduce(plan, b_src, b_dst)  # noqa: E731
+        if k == "rs_ar_reduce_apply":
+            sg = alloc(shard_sizes, gdt)
+            b_sg = plan.bind("shard_grads", gdt, sg)
+            dst = dst + sg
+            call = lambda: C.fsdp_rs_ar_reduce_apply(plan, b_src, b_dst, "avg", b_sg)  # noqa: E731
     else:
         src = alloc([plan.slice_numel("f32")] * W, "f32")
         WL.torch_fill_(src, wl.seed_grads, wl.grad_std, "f32")

@@ -1325,6 +1325,13 @@ template <typename S, int NS, int SIN, int ND>
 __global__ void __launch_bounds__(sm_warps<K_RSAR, S, NS, ND>() * 32, 1) rs_ar_reduce_sm_kernel(const KArgs a) {
     staged_reduce_body<K_RSAR, S, NS, SIN, ND, kSmRG>(a);
 }
+// Per SM, with the apply folded in: each stage also holds D gradient
+// pointers, sized like a reduce with twice the destinations.
+template <typename S, int NS, int SIN, int ND>
+__global__ void __launch_bounds__(sm_warps<K_RSAR, S, NS, 2 * ND>() * 32, 1)
+    rs_ar_reduce_apply_sm_kernel(const KArgs a) {
+    staged_reduce_body<K_RSAR, S, NS, SIN, ND, kSmRG, true>(a);
+}
 template <typename S, int NS>
 __global__ void __launch_bounds__(sm_warps<K_RS, S, NS, 1>() * 32, 1) rs_reduce_sm_kernel(const KArgs a) {
     staged_reduce_body<K_RS, S, NS, NS, 1, kSmRG>(a);
@@ -1613,6 +1620,20 @@ cudaError_t launch(Kind kind, int sdt, int ddt, const KArgs& a, cudaStream_t st)
             return sf ? go(rs_copy_in_kernel<float>, a, st)
                       : go(rs_copy_in_kernel<uint16_t>, a, st, kThreads, 0, FSDP_GRID_RSIN);
         case K_RSAR:
+            if (a.sg_tab && a.max_grid > 0) {
+                // the apply folded in, on a capped grid: one block per SM
+                if (sf)
+                    return go_sm<float>(rs_ar_reduce_apply_sm_kernel<float, 0, 0, 0>, a, st, a.W, 2 * a.D, false,
+                                        sm_warps<K_RSAR, float, 0, 0>());
+#define FSDP_RSAR_AP_SM(W_, S_)                                                                               \
+    if (a.W == W_ && a.S == S_)                                                                               \
+        return go_sm<uint16_t>(rs_ar_reduce_apply_sm_kernel<uint16_t, W_, S_, W_ / S_>, a, st, W_, 2 * (W_ / S_), \
+                               fan_out<K_RSAR, W_, W_ / S_>(), sm_warps<K_RSAR, uint16_t, W_, 2 * (W_ / S_)>());
+                FSDP_RSAR_AP_SM(16, 8) FSDP_RSAR_AP_SM(8, 4) FSDP_RSAR_AP_SM(8, 8) FSDP_RSAR_AP_SM(8, 1)
+#undef FSDP_RSAR_AP_SM
+                return go_sm<uint16_t>(rs_ar_reduce_apply_sm_kernel<uint16_t, 0, 0, 0>, a, st, a.W, 2 * a.D, false,
+                                       sm_warps<K_RSAR, uint16_t, 0, 0>());
+            }
             if (a.sg_tab) {
                 // the apply folded in (can_fold_apply said the shape fits);
                 // each stage holds 2 * D destination pointers

@@ -160,18 +160,22 @@ class BackwardPipeline:
     fused kernel on the shard stream and are applied at the end. No call
     blocks the host; finish() waits on the host with a time limit."""
 
-    def __init__(self, units, op="avg", fused=False, comm_blocks=0, sync_priority=-1):
+    def __init__(self, units, op="avg", fused=False, comm_blocks=0, sync_priority=-1, one_pass=False):
         """comm_blocks > 0 caps the thread blocks of every sync kernel the
         pipeline issues on its sync streams (fsdp_plan_set_grid_limit; the
         reduces then run one block per SM), leaving the other SMs to the
         backward compute; the applies on the compute stream keep the whole
-        GPU. sync_priority is the sync streams' priority:
+        GPU. one_pass (fused only): each layer's sync is the fused reduce
+        with the apply folded in (fsdp_rs_ar_reduce_apply) on the shard
+        stream, so nothing is left to apply at the root (same bits).
+        sync_priority is the sync streams' priority:
         -1 (high, the default) places their blocks as soon as SMs free up;
         0 (the compute stream's) lets compute blocks go first."""
         self.units = list(units)
         self.op = op
         self.fused = fused
         self.comm_blocks = comm_blocks
+        self.one_pass = bool(one_pass) and bool(fused)
         dev = self.units[0].device if self.units else torch.device("cuda")
         self.rs_stream = torch.cuda.Stream(device=dev, priority=sync_priority)
         self.ar_stream = torch.cuda.Stream(device=dev, priority=sync_priority)
@@ -218,13 +222,17 @@ class BackwardPipeline:
                     self._apply(prev, comp)
             self.rs_stream.wait_event(ev_grad)                     # step 3
             with torch.cuda.stream(self.rs_stream):
-                if self.fused:
+                if self.one_pass:
+                    self.units[L].reduce_grads_one_pass(self.op)
+                elif self.fused:
                     self.units[L].rs_ar_reduce()
                 else:
                     self.units[L].rs(self.op)
             self.log.append(("rs", L))
             ev_rs[L] = self.rs_stream.record_event()
-            if self.fused:
+            if self.one_pass:
+                self.log.append(("apply", L))
+            elif self.fused:
                 pending_apply.append(L)
             elif prev is not None and self.units[prev].plan.D > 1:  # step 4
                 self.ar_stream.wait_event(ev_rs[prev])

@@ -2,8 +2,9 @@
 "Hyper通信掩盖方案" PR #758 write-up §二.2) and CUDA-graph replay of a step.
 
 The pipeline's applied shard gradients are compared byte for byte with the
-CPU oracle: the fused path with the oracle's RS copy-in + fused reduce +
-apply (AVG divides by W once), the unfused path with the oracle's unfused
+CPU oracle: the fused path (and its one-pass form, the apply folded into
+the fused reduce) with the oracle's RS copy-in + fused reduce + apply (AVG
+divides by W once), the unfused path with the oracle's unfused
 steps (ReduceScatter with AVG over the shard group, AllReduce with AVG over
 the replicas, apply SUM). Both run with the sync kernels on the whole GPU
 and with their grid capped to a few SMs (one block per SM of many warps)."""
@@ -51,7 +52,7 @@ def oracle_shard_grads(layer, grads, op, fused):
 
 
 @pytest.mark.parametrize("comm_blocks", [0, 6])
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "one_pass"])
 @pytest.mark.parametrize("op", ["avg", "sum"])
 def test_pipelined_backward_matches_oracle(fused, op, comm_blocks):
     units, truth = build_stack()
@@ -68,7 +69,9 @@ def test_pipelined_backward_matches_oracle(fused, op, comm_blocks):
         for g, v in zip(units[L].grads, truth[L]):  # "produce" the gradients
             g.copy_(v)
 
-    pipe = BackwardPipeline(units, op=op, fused=fused, comm_blocks=comm_blocks)
+    one_pass = fused == "one_pass"
+    fused = bool(fused)
+    pipe = BackwardPipeline(units, op=op, fused=fused, comm_blocks=comm_blocks, one_pass=one_pass)
     done = pipe.run(backward_compute)
     BackwardPipeline.finish(done, timeout_s=60)
     for L, u in enumerate(units):
