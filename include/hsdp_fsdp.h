@@ -36,8 +36,9 @@
  *     allocated by fsdp_plan_upload / fsdp_bind and freed by the matching
  *     destroy). Data calls never allocate, never free, never synchronise.
  *   - Streams: data calls enqueue exactly one kernel on `stream` (NULL = the
- *     legacy default stream) and return; launch failures come back as
- *     FSDP_ERR_CUDA. Calls on different streams are safe when the buffers
+ *     legacy default stream; fsdp_rs_ar_reduce_apply on a mesh too wide for
+ *     its one-pass kernel enqueues the two it stands for) and return;
+ *     launch failures come back as FSDP_ERR_CUDA. Calls on different streams are safe when the buffers
  *     they write are disjoint from the buffers the others touch.
  *   - Pointers: device pointers aligned to their element size; NULL only
  *     for a buffer of 0 elements. 16-byte-aligned pointers (every PyTorch

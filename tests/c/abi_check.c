@@ -226,6 +226,44 @@ int main(void) {
         }
     }
 
+    /* the sync in one pass: the same fused regions and shard gradients from
+     * one kernel, on buffers dirtied first */
+    for (int op = FSDP_AVG; op <= FSDP_SUM; ++op) {
+        for (int w = 0; w < W; ++w) CUDA(cudaMemset(fused[w], 0xFF, (size_t)n_fused[w] * 4));
+        for (int i = 0; i < W * P; ++i)
+            if (n_shard[i]) CUDA(cudaMemset(sgrad[i], 0xFF, (size_t)n_shard[i] * 2));
+        const uint64_t l1 = fsdp_launch_count();
+        OK(fsdp_rs_ar_reduce_apply(plan, b_grads, b_fused, op, 0, b_sgrad, NULL));
+        CUDA(cudaDeviceSynchronize());
+        CHECK(fsdp_launch_count() - l1 == 1, "one-pass launches %llu", (unsigned long long)(fsdp_launch_count() - l1));
+        for (int w = 0; w < W; ++w) {
+            const int s = w % S;
+            float* f = (float*)malloc((size_t)n_fused[w] * 4);
+            CUDA(cudaMemcpy(f, fused[w], (size_t)n_fused[w] * 4, cudaMemcpyDeviceToHost));
+            for (int64_t j = 0; j < n_fused[w]; ++j) {
+                float want = 0.0f;
+                for (int p = 0; p < P; ++p)
+                    if (j >= o[p] && j < o[p] + len[p][s] * INNER[p])
+                        want = (float)(10 * (1 + (off[p][s] * INNER[p] + (j - o[p])) % 3));
+                CHECK(memcmp(&f[j], &want, 4) == 0, "one-pass fused[%d][%lld] = %g, want %g", w, (long long)j, f[j],
+                      want);
+            }
+            free(f);
+        }
+        for (int i = 0; i < W * P; ++i) {
+            const int w = i / P, p = i % P, s = w % S;
+            uint16_t* h = (uint16_t*)malloc((size_t)(n_shard[i] ? n_shard[i] : 1) * 2);
+            CUDA(cudaMemcpy(h, sgrad[i], (size_t)n_shard[i] * 2, cudaMemcpyDeviceToHost));
+            for (int64_t k = 0; k < n_shard[i]; ++k) {
+                const float sum = (float)(10 * (1 + (off[p][s] * INNER[p] + k) % 3));
+                const uint16_t want = bf16(op == FSDP_AVG ? sum / W : sum);
+                CHECK(h[k] == want, "one-pass %s shard grad[%d][%lld] = %04x, want %04x",
+                      op == FSDP_AVG ? "AVG" : "SUM", i, (long long)k, h[k], want);
+            }
+            free(h);
+        }
+    }
+
     OK(fsdp_binding_destroy(b_shards));
     OK(fsdp_binding_destroy(b_ag));
     OK(fsdp_binding_destroy(b_full));
