@@ -315,6 +315,9 @@ def fsdp_rs_ar_reduce_noalloc(plan, grad_dt, grads, fused, stream=None):
     as pointer arrays on every call. The library cannot see the tensors'
     sizes here, so their count, dtype and size are checked before the call."""
     P = plan.P
+    # both counts first (the library reads both arrays), then each tensor
+    _check_tensors("rs_ar_reduce_noalloc grads", grads, plan.W * P, None)
+    _check_tensors("rs_ar_reduce_noalloc fused", fused, plan.W, None)
     _check_tensors("rs_ar_reduce_noalloc grads", grads, plan.W * P, grad_dt, lambda i: plan.numel(i % P))
     sf = plan.slice_numel("f32")
     _check_tensors("rs_ar_reduce_noalloc fused", fused, plan.W, "f32", lambda i: sf)

@@ -177,3 +177,26 @@ def test_error_messages_are_per_thread():
     for t in threads:
         t.join()
     assert errors == [] and len(results) == 8
+
+
+def test_pointer_lists_are_checked_before_the_library_reads_them():
+    # the library reads W*P (or W) pointers from the arrays it is given; the
+    # binding refuses a list of another length, and for the allocation-free
+    # call also tensors of the wrong dtype or not on a GPU, before any call
+    import torch
+
+    plan = C.Plan([7, 16], [8, 1], 4, 2)  # host-only: no GPU needed
+    g = torch.zeros(8, dtype=torch.bfloat16)
+    f = torch.zeros(plan.slice_numel("f32"), dtype=torch.float32)
+    with pytest.raises(C.FsdpError, match="tensors given"):
+        C.fsdp_rs_ar_reduce_noalloc(plan, "bf16", [g] * 7, [f] * 4)
+    with pytest.raises(C.FsdpError, match="tensors given"):
+        C.fsdp_rs_ar_reduce_noalloc(plan, "bf16", [g] * 8, [f] * 3)
+    with pytest.raises(C.FsdpError, match="expected contiguous"):  # CPU tensors
+        C.fsdp_rs_ar_reduce_noalloc(plan, "bf16", [g] * 8, [f] * 4)
+    with pytest.raises(C.FsdpError, match="expected contiguous"):  # wrong dtype
+        C.fsdp_rs_ar_reduce_noalloc(plan, "bf16", [g.float()] * 8, [f] * 4)
+    with pytest.raises(C.FsdpError, match="tensors given"):
+        C.Binding(plan, "grads", "bf16", [g] * 3)
+    with pytest.raises(C.FsdpError, match="tensors given"):
+        C.Binding(plan, "fused", "f32", [f] * 5, check_sizes=False)
