@@ -65,8 +65,10 @@ def parse(argv=None):
                     help="the small case of an ncu capture: only this kernel, --launches times, on the "
                          "workload scaled by --scale with only its buffers allocated (prints no bench line)")
     ap.add_argument("--launches", type=int, default=3)
-    ap.add_argument("--pipeline", type=int, default=0, metavar="LAYERS",
-                    help="also measure the pipelined backward over LAYERS layers of the workload")
+    ap.add_argument("--pipeline", type=int, default=4, metavar="LAYERS",
+                    help="also measure the pipelined backward over LAYERS layers of --pipeline-workload "
+                         "(0: skip)")
+    ap.add_argument("--pipeline-workload", default="hsdp_2x4_llama")
     return ap.parse_args(argv)
 
 
@@ -561,7 +563,8 @@ def run_gpu(args, wl):
 
     per_workload = None
     want_per = not args.no_per_workload and args.scale == 1.0 and wl.key == "large_hsdp"
-    if args.pipeline or want_per:
+    want_pipe = args.pipeline > 0 and args.scale == 1.0
+    if want_pipe or want_per:
         unit.close()
         del unit
         torch.cuda.empty_cache()
@@ -569,8 +572,8 @@ def run_gpu(args, wl):
         per_workload = run_per_workload(args, dev, peak)
 
     pipeline = None
-    if args.pipeline:
-        pipeline = run_pipeline(args, wl, d0, dev)
+    if want_pipe:
+        pipeline = run_pipeline(args, dev)
 
     cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -598,7 +601,7 @@ def run_gpu(args, wl):
         if pipeline:
             line["pipeline"] = pipeline
         print(json.dumps(line), flush=True)
-    if not (args.pipeline or want_per):
+    if not (want_pipe or want_per):
         unit.close()
     return 0
 
@@ -688,21 +691,28 @@ def run_per_workload(args, dev, peak):
     return out
 
 
-def run_pipeline(args, wl, d0, dev):
+def run_pipeline(args, dev):
     """Overlap of the gradient sync with backward compute over a stack of
-    layers: the stand-in backward of a layer is bf16 GEMMs on the compute
-    stream sized to take about as long as that layer's sync; the sync runs
-    the pages' 4-step pipeline (unfused) or the fused kernel per layer."""
+    layers ("Hyper通信掩盖方案" PR #758 write-up §二.2: the 4-step pipeline):
+    the stand-in backward of a layer is bf16 GEMMs (8192^3, cuBLAS) on the
+    compute stream, as many as take about one layer's sync; the sync runs
+    as the pages' unfused 4-step schedule, as the fused reduce (+ apply at
+    the root), or as the one-pass fused sync per layer. Each is timed alone
+    (whole GPU), serially after the compute, and pipelined with its kernels
+    capped at `cap` blocks while compute runs beside them (one block per SM,
+    on the high-priority sync streams; cap 0 = the whole-GPU kernels).
+    hidden = (compute + sync - pipelined) / min(compute, sync)."""
     import torch
 
     from hsdp_sharded_parameter_gb300 import capi as C
     from hsdp_sharded_parameter_gb300 import workloads as WL
     from hsdp_sharded_parameter_gb300.runtime import BackwardPipeline, HsdpUnit
 
+    wl = WL.WORKLOADS[args.pipeline_workload]
     n = args.pipeline
     units = []
     for i in range(n):
-        u = HsdpUnit(C.Plan(d0, wl.inner, wl.rank_size, wl.shard_size).upload(), wl.param_dtype,
+        u = HsdpUnit(C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).upload(), wl.param_dtype,
                      wl.grad_dtype, device=dev, with_unfused=True)
         WL.torch_fill_(u.grads, wl.seed_grads + 100 * i, wl.grad_std, wl.grad_dtype)
         units.append(u)
@@ -720,6 +730,10 @@ def run_pipeline(args, wl, d0, dev):
         torch.cuda.synchronize()
         return s.elapsed_time(e) / reps
 
+    def set_cap(cap):
+        for u in units:
+            u.plan.set_grid_limit(cap)
+
     # size the stand-in backward of one layer to about one layer's fused sync
     t_sync1 = timed(lambda: units[0].reduce_grads("avg"))
     t_mm = timed(lambda: torch.mm(a, a))
@@ -729,28 +743,30 @@ def run_pipeline(args, wl, d0, dev):
         for _ in range(k):
             torch.mm(a, a)
 
-    out = {"layers": n, "workload": wl.key, "gemms_per_layer": k, "gemm": "8192^3 bf16"}
+    out = {"layers": n, "workload": wl.key, "gemms_per_layer": k, "gemm": "8192^3 bf16 (cuBLAS)",
+           "caps": "blocks of each sync kernel issued while compute may run (one per SM); 0 = whole GPU"}
     t_comp = timed(lambda: [compute(L) for L in reversed(range(n))])
     out["compute_only_ms"] = round(t_comp, 3)
-    for mode in ("fused", "one_pass", "unfused"):
-        fused, one = mode != "unfused", mode == "one_pass"
-        name = {"fused": "fused", "one_pass": "fused_one_pass", "unfused": "unfused_4step"}[mode]
-        if one:
-            t_sync = timed(lambda: [units[L].reduce_grads_one_pass("avg") for L in reversed(range(n))])
-        elif fused:
-            t_sync = timed(lambda: [units[L].reduce_grads("avg") for L in reversed(range(n))])
-        else:
-            t_sync = timed(lambda: [units[L].reduce_grads_unfused("avg") for L in reversed(range(n))])
+    syncs = {"one_pass": lambda L: units[L].reduce_grads_one_pass("avg"),
+             "fused": lambda L: units[L].reduce_grads("avg"),
+             "unfused_4step": lambda L: units[L].reduce_grads_unfused("avg")}
+    for mode, sync in syncs.items():
+        fused, one = mode != "unfused_4step", mode == "one_pass"
+        t_sync = timed(lambda: [sync(L) for L in reversed(range(n))])
         res = {"sync_only_ms": round(t_sync, 3), "serial_ms": round(t_comp + t_sync, 3)}
-        # sync kernels on the whole GPU (0) or on a capped number of blocks
-        for cap in (0, 64, 96, 112, 128):
+        for cap in (0, 48, 56, 64, 80):
+            row = {}
+            if cap:
+                set_cap(cap)
+                row["sync_only_capped_ms"] = round(timed(lambda: [sync(L) for L in reversed(range(n))]), 3)
+                set_cap(0)
             t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, comm_blocks=cap, one_pass=one).run(compute))
-            hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
-            res[f"comm_blocks_{cap}"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
-        t_pipe = timed(lambda: BackwardPipeline(units, "avg", fused, sync_priority=0, one_pass=one).run(compute))
-        hidden = (t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync))
-        res["sync_low_priority"] = {"pipelined_ms": round(t_pipe, 3), "hidden_frac": round(hidden, 3)}
-        out[name] = res
+            row["pipelined_ms"] = round(t_pipe, 3)
+            row["hidden_frac"] = round((t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync)), 3)
+            res[f"cap_{cap}"] = row
+        out[mode] = res
+    status = [u.plan.status() for u in units]
+    out["status_words"] = status
     for u in units:
         u.close()
     return out

@@ -1,7 +1,8 @@
 """Builds the C-ABI library ``lib/libhsdp_fsdp.so`` in-tree.
 
-Three translation units compiled in parallel and linked with nvcc:
+Four translation units compiled in parallel and linked with nvcc:
   * csrc/fsdp_kernels.cu -- the sm_103a kernels (nvcc, one -gencode)
+  * csrc/fsdp_bulk.cu    -- the bulk-fed fused reduce of a capped grid
   * csrc/fsdp_noalloc.cu -- the allocation-free fused gradient sync
   * csrc/fsdp_capi.cpp   -- plan, bindings and entry points (host C++)
 No fast-math, no FMA contraction, no flush-to-zero: the kernels' additions,
@@ -48,12 +49,15 @@ def build(verbose: bool = False, extra_nvcc=()) -> str:
     tag = str(os.getpid())
     obj_k = os.path.join(LIB_DIR, f"fsdp_kernels.{tag}.o")
     obj_n = os.path.join(LIB_DIR, f"fsdp_noalloc.{tag}.o")
+    obj_b = os.path.join(LIB_DIR, f"fsdp_bulk.{tag}.o")
     obj_c = os.path.join(LIB_DIR, f"fsdp_capi.{tag}.o")
     jobs = [
         [nvcc, *ARCH, *NVCC_FLAGS, *extra_nvcc, *inc, "-c", os.path.join(CSRC, "fsdp_kernels.cu"),
          "-o", obj_k],
         [nvcc, *ARCH, *NVCC_FLAGS, *extra_nvcc, *inc, "-c", os.path.join(CSRC, "fsdp_noalloc.cu"),
          "-o", obj_n],
+        [nvcc, *ARCH, *NVCC_FLAGS, *extra_nvcc, *inc, "-c", os.path.join(CSRC, "fsdp_bulk.cu"),
+         "-o", obj_b],
         ["g++", *CXX_FLAGS, *inc, "-I", os.path.join(cuda, "include"), "-c",
          os.path.join(CSRC, "fsdp_capi.cpp"), "-o", obj_c],
     ]
@@ -68,10 +72,10 @@ def build(verbose: bool = False, extra_nvcc=()) -> str:
     if failed:
         raise RuntimeError("compile failed: " + "; ".join(failed))
     tmp = os.path.join(LIB_DIR, f"{LIB_NAME}.{tag}")
-    subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "shared", obj_k, obj_n, obj_c, "-o", tmp,
+    subprocess.run([nvcc, *ARCH, "-shared", "-cudart", "shared", obj_k, obj_n, obj_b, obj_c, "-o", tmp,
                     "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")], check=True)
     os.replace(tmp, library_path())
-    for o in (obj_k, obj_n, obj_c):
+    for o in (obj_k, obj_n, obj_b, obj_c):
         os.remove(o)
     return library_path()
 

@@ -20,6 +20,7 @@ from .build import library_path
 FSDP_OK, FSDP_ERR_INVALID_ARG, FSDP_ERR_NOT_IMPLEMENTED, FSDP_ERR_CUDA, FSDP_ERR_NOMEM = range(5)
 FSDP_F32, FSDP_BF16 = 0, 1
 FSDP_AVG, FSDP_SUM = 0, 1
+FSDP_STATUS_PRODUCER_WAIT, FSDP_STATUS_CONSUMER_WAIT, FSDP_STATUS_ORDER = 1, 2, 4
 (FSDP_ROLE_SHARDS, FSDP_ROLE_AG_OUTPUT, FSDP_ROLE_FULL_PARAMS, FSDP_ROLE_GRADS,
  FSDP_ROLE_RS_INPUT, FSDP_ROLE_FUSED, FSDP_ROLE_SHARD_GRADS) = range(7)
 
@@ -68,6 +69,9 @@ def lib():
         L.fsdp_plan_destroy.argtypes = [vp]
         L.fsdp_plan_upload.argtypes = [vp]
         L.fsdp_plan_set_grid_limit.argtypes = [vp, i32]
+        L.fsdp_plan_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+        L.fsdp_plan_inject_stall.argtypes = [vp, i32]
+        L.fsdp_plan_status.argtypes = [vp, vp, P(i32)]
         L.fsdp_plan_check_tables.argtypes = [vp]
         L.fsdp_plan_info.argtypes = [vp, P(i32), P(i32), P(i32), P(i32), P(i64)]
         L.fsdp_slice_numel.argtypes = [vp, i32, P(i64)]
@@ -158,6 +162,22 @@ class Plan:
     def set_grid_limit(self, max_blocks):
         _check(lib().fsdp_plan_set_grid_limit(self.handle, int(max_blocks)))
         return self
+
+    def set_wait_limit(self, nanoseconds):
+        _check(lib().fsdp_plan_set_wait_limit(self.handle, int(nanoseconds)))
+        return self
+
+    def inject_stall(self, on=True):
+        _check(lib().fsdp_plan_inject_stall(self.handle, int(bool(on))))
+        return self
+
+    def status(self, stream=None):
+        """The plan's status word after the calls enqueued on `stream` (the
+        stream is synchronised; the word is cleared): 0, or the
+        FSDP_STATUS_* bits of waits that ran out."""
+        v = ctypes.c_int(0)
+        _check(lib().fsdp_plan_status(self.handle, _stream(stream), ctypes.byref(v)))
+        return v.value
 
     def slice_numel(self, dt):
         out = ctypes.c_int64()

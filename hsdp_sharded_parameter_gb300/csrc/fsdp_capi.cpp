@@ -278,6 +278,9 @@ KArgs base_args(const fsdp_plan_s* pl, TableId t, int reps) {
     a.W = pl->W;
     a.max_grid = pl->max_grid;
     a.staged_blocks = pl->staged_blocks;
+    a.status = pl->dev_status;
+    a.wait_ns = pl->wait_ns;
+    a.stall = pl->stall;
     set_divisor(a, 1);
     return a;
 }
@@ -417,6 +420,9 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
         mapped[t] = segs[t].size() > kMapMinRuns;
         if (mapped[t]) bytes += ((size_t)tiles[t].back() * sizeof(int32_t) + 255) / 256 * 256;
     }
+    // the status word of the kernels that wait inside (zero: nothing ran out)
+    const size_t status_at = bytes;
+    bytes += 256;
     std::vector<unsigned char> host(bytes, 0);
     for (int t = 0; t < T_COUNT; ++t) {
         if (!segs[t].empty()) std::memcpy(&host[seg_at[t]], segs[t].data(), segs[t].size() * sizeof(Seg));
@@ -435,6 +441,7 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
         return cuda_fail(e, "plan_upload");
     }
     pl->dev_block = block;
+    pl->dev_status = reinterpret_cast<int*>(static_cast<char*>(block) + status_at);
     for (int t = 0; t < T_COUNT; ++t) {
         pl->tables[t].segs = reinterpret_cast<const Seg*>(static_cast<char*>(block) + seg_at[t]);
         pl->tables[t].tile_begin = reinterpret_cast<const int64_t*>(static_cast<char*>(block) + tile_at[t]);
@@ -522,6 +529,35 @@ int fsdp_plan_set_grid_limit(fsdp_plan_t pl, int max_blocks) {
     FSDP_CHECK_PLAN(pl);
     if (max_blocks < 0) return set_error(FSDP_ERR_INVALID_ARG, "plan_set_grid_limit: max_blocks must be >= 0");
     pl->max_grid = max_blocks;
+    return FSDP_OK;
+}
+
+int fsdp_plan_set_wait_limit(fsdp_plan_t pl, uint64_t nanoseconds) {
+    clear_error();
+    FSDP_CHECK_PLAN(pl);
+    pl->wait_ns = nanoseconds ? nanoseconds : 1000000000ull;
+    return FSDP_OK;
+}
+
+int fsdp_plan_inject_stall(fsdp_plan_t pl, int on) {
+    clear_error();
+    FSDP_CHECK_PLAN(pl);
+    pl->stall = on ? 1 : 0;
+    return FSDP_OK;
+}
+
+int fsdp_plan_status(fsdp_plan_t pl, fsdp_stream_t stream, int* status) {
+    clear_error();
+    int rc;
+    if ((rc = check_ready(pl, "plan_status"))) return rc;
+    if (!status) return set_error(FSDP_ERR_INVALID_ARG, "plan_status: status is NULL");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, pl->dev_status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(pl->dev_status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan_status");
+    *status = v;
     return FSDP_OK;
 }
 

@@ -107,6 +107,14 @@ struct KArgs {
     // The fused reduce with the apply folded in: the [W][P] table of
     // actual-shard gradients it also writes (nullptr: not folded in).
     void* const* sg_tab;
+    // Kernels that wait inside (the bulk-fed reduce of a capped grid): the
+    // plan's device status word (nullptr: such kernels are not used), the
+    // limit of any one wait in nanoseconds, and the failure-detection test
+    // hook (nonzero: block 0 never announces its first chunk, so that waits
+    // for it run out).
+    int* status;
+    uint64_t wait_ns;
+    int stall;
 };
 
 // Fills div, scale_mode and recip for a divisor d >= 1.
@@ -136,6 +144,17 @@ cudaError_t launch(Kind kind, int src_dt, int dst_dt, const KArgs& a, cudaStream
 // the apply in (its staged form fits with the replicas' gradient pointers).
 bool can_fold_apply(int src_dt, int W, int D);
 
+// The fused reduce (K_RSAR, with the apply folded in when a.sg_tab is set)
+// on a capped grid, fed by TMA bulk loads (fsdp_bulk.cu). Sets *used to
+// false, launching nothing, when the shape does not fit its shared-memory
+// ring (the caller then takes the staged kernels).
+cudaError_t launch_bulk_reduce(int src_dt, const KArgs& a, cudaStream_t stream, bool* used);
+
+// Status bits a kernel with internal waits sets in the plan's status word.
+constexpr int kStatusProducerWait = 1;  // a stage was not released in time
+constexpr int kStatusConsumerWait = 2;  // a stage's data did not arrive in time
+constexpr int kStatusOrder = 4;         // a consumer found another chunk's record (internal error)
+
 }  // namespace fsdp
 
 struct fsdp_plan_s {
@@ -145,6 +164,9 @@ struct fsdp_plan_s {
     int device = -1;
     bool uploaded = false;
     int max_grid = 0;  // fsdp_plan_set_grid_limit
+    uint64_t wait_ns = 1000000000ull;  // fsdp_plan_set_wait_limit
+    int stall = 0;                     // fsdp_plan_inject_stall
+    int* dev_status = nullptr;         // inside dev_block
     int staged_blocks = 2;  // see KArgs::staged_blocks, set by fsdp_plan_upload
     bool agout_shifted = false;  // see KArgs::shifted (bf16 copy-out), set by fsdp_plan_upload
     void* dev_block = nullptr;

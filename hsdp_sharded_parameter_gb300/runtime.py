@@ -162,10 +162,14 @@ class BackwardPipeline:
 
     def __init__(self, units, op="avg", fused=False, comm_blocks=0, sync_priority=-1, one_pass=False):
         """comm_blocks > 0 caps the thread blocks of every sync kernel the
-        pipeline issues on its sync streams (fsdp_plan_set_grid_limit; the
-        reduces then run one block per SM), leaving the other SMs to the
-        backward compute; the applies on the compute stream keep the whole
-        GPU. one_pass (fused only): each layer's sync is the fused reduce
+        pipeline issues on its sync streams while backward compute may still
+        run beside it (fsdp_plan_set_grid_limit; the reduces then run one
+        block per SM), leaving the other SMs to the backward compute; the
+        compute should leave those SMs free (torch's cuBLAS SM carveout does
+        that for GEMMs). The syncs issued after the last layer's backward
+        (layer 0's ReduceScatter or fused sync, the root's AllReduce) and
+        the applies on the compute stream have nothing to share the GPU
+        with and run uncapped. one_pass (fused only): each layer's sync is the fused reduce
         with the apply folded in (fsdp_rs_ar_reduce_apply) on the shard
         stream, so nothing is left to apply at the root (same bits).
         sync_priority is the sync streams' priority:
@@ -221,6 +225,8 @@ class BackwardPipeline:
                 if self.units[prev].plan.D == 1:                   # step 2
                     self._apply(prev, comp)
             self.rs_stream.wait_event(ev_grad)                     # step 3
+            if L == 0:  # no backward compute left beside it
+                self.units[L].plan.set_grid_limit(0)
             with torch.cuda.stream(self.rs_stream):
                 if self.one_pass:
                     self.units[L].reduce_grads_one_pass(self.op)

@@ -138,8 +138,9 @@ int fsdp_plan_destroy(fsdp_plan_t plan);
 /* Uploads the plan's work tables to the current CUDA device (synchronous,
  * allocates device memory once: 40 bytes per run of each kernel's table,
  * plus, for tables of more than 1024 runs, 4 bytes per 2048 elements the
- * table covers). Required before any data call; data calls must then run
- * with that device current. Calling it again is a no-op. */
+ * table covers, plus the plan's 4-byte status word, see fsdp_plan_status).
+ * Required before any data call; data calls must then run with that device
+ * current. Calling it again is a no-op. */
 int fsdp_plan_upload(fsdp_plan_t plan);
 
 /* Caps the number of thread blocks every later data call of this plan
@@ -148,10 +149,43 @@ int fsdp_plan_upload(fsdp_plan_t plan);
  * gives the same results; a small cap leaves the other SMs to kernels
  * running beside them, e.g. the backward compute the gradient sync overlaps
  * with, the way the pages' communication streams run beside compute
- * [OVERLAP §二.2]. Under a cap the reductions (fused RS+AR, ReduceScatter,
- * AllReduce) run one block per SM with up to 16 warps, so max_blocks is
- * the number of SMs they occupy. May be changed between calls. */
+ * [OVERLAP §二.2]. Under a cap the reductions run one block per SM, so
+ * max_blocks is the number of SMs they occupy: the fused RS+AR (with or
+ * without the apply folded in) as a producer warp feeding eight folding
+ * warps through TMA bulk loads into a shared-memory ring (up to 32 sources
+ * of bf16, 16 of fp32; its waits are bounded, see fsdp_plan_status), the
+ * unfused ReduceScatter and AllReduce (and a fused reduce with more
+ * sources) with up to 16 warps of per-warp cp.async rings. May be changed
+ * between calls. */
 int fsdp_plan_set_grid_limit(fsdp_plan_t plan, int max_blocks);
+
+/* Failure detection of the kernels that wait inside (the bulk-fed fused
+ * reduce of a capped grid; no counterpart in the pages, whose collectives
+ * report errors through HCCL). Each such wait gives up after `nanoseconds`
+ * (default 1 s; 0 restores the default): the block then records why in
+ * the plan's status word, stops, waits (bounded too) for its copies in
+ * flight, and the kernel returns, so the CUDA context stays usable and the
+ * outputs of that call are undefined. */
+int fsdp_plan_set_wait_limit(fsdp_plan_t plan, uint64_t nanoseconds);
+
+/* Reads the plan's status word after every call enqueued on `stream` so far
+ * (synchronises the stream), stores it in *status and clears it. 0: no
+ * wait ran out; otherwise FSDP_STATUS_PRODUCER_WAIT (a stage of the ring was
+ * not released in time), FSDP_STATUS_CONSUMER_WAIT (a stage's data did not
+ * arrive in time) and/or FSDP_STATUS_ORDER (a folding warp found the record
+ * of another chunk than the one it waited for and stopped before storing:
+ * an internal error). Returns FSDP_ERR_CUDA if the copy fails. */
+#define FSDP_STATUS_PRODUCER_WAIT 1
+#define FSDP_STATUS_CONSUMER_WAIT 2
+#define FSDP_STATUS_ORDER 4
+int fsdp_plan_status(fsdp_plan_t plan, fsdp_stream_t stream, int* status);
+
+/* Test hook of that failure detection: with on != 0, every later bulk-fed
+ * reduce of this plan withholds the first chunk of its first block, so the
+ * waits for it run out after the wait limit and set the status word (the
+ * call's outputs are then undefined). No fault, trap or endless wait is
+ * involved. 0 switches it off. */
+int fsdp_plan_inject_stall(fsdp_plan_t plan, int on);
 
 /* Diagnostic, with no counterpart in the pages: builds the plan's work
  * tables on the host, as fsdp_plan_upload does, and checks every run
