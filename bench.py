@@ -65,6 +65,8 @@ def parse(argv=None):
                     help="the small case of an ncu capture: only this kernel, --launches times, on the "
                          "workload scaled by --scale with only its buffers allocated (prints no bench line)")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--grid-limit", type=int, default=0,
+                    help="with --profile-kernel: cap the kernel's blocks (fsdp_plan_set_grid_limit)")
     ap.add_argument("--pipeline", type=int, default=4, metavar="LAYERS",
                     help="also measure the pipelined backward over LAYERS layers of --pipeline-workload "
                          "(0: skip)")
@@ -896,15 +898,20 @@ def run_profile_case(args, wl):
         dst = alloc(shard_sizes, gdt)
         b_src, b_dst = plan.bind("fused", "f32", src), plan.bind("shard_grads", gdt, dst)
         call = lambda: C.fsdp_apply_grads(plan, b_src, "avg", b_dst)  # noqa: E731
+    plan.set_grid_limit(args.grid_limit)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     for i in range(args.launches):
         ev[0].record()
         call()
         ev[1].record()
         torch.cuda.synchronize()
-        print(f"{k} {wl.key} dim0 x{args.scale:g} launch {i}: {ev[0].elapsed_time(ev[1]) * 1e3:.1f} us",
-              flush=True)
+        print(f"{k} {wl.key} dim0 x{args.scale:g} grid limit {args.grid_limit} launch {i}: "
+              f"{ev[0].elapsed_time(ev[1]) * 1e3:.1f} us", flush=True)
     print(f"{k}: {sum(t.numel() * t.element_size() for t in src + dst) / 1e9:.2f} GB on the device", flush=True)
+    status = plan.status()
+    if status:
+        print(f"{k}: plan status {status} (a wait inside the kernel ran out)", flush=True)
+        return 1
     return 0
 
 

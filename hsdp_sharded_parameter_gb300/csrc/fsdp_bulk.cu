@@ -562,10 +562,14 @@ cudaError_t go_bulk(const KArgs& a, cudaStream_t st) {
 // and there are at most two replicas (with 8 replicas, the pure-TP layer,
 // one group measured faster: 0.529 against 0.408 of the measured copy peak
 // on 64 SMs).
+#ifndef FSDP_BULK_GROUPS
+#define FSDP_BULK_GROUPS 0  // 0: by the rule above; 1 or 2: always that many
+#endif
 template <typename S, int NS, int SIN, int ND, bool AP>
 cudaError_t go_bulk_shape(const KArgs& a, cudaStream_t st) {
-    return bulk_stages<S, 2>(a.W) >= 4 && a.D <= 2 ? go_bulk<S, NS, SIN, ND, AP, 2>(a, st)
-                                                    : go_bulk<S, NS, SIN, ND, AP, 1>(a, st);
+    const bool two = FSDP_BULK_GROUPS == 2 || (FSDP_BULK_GROUPS == 0 && bulk_stages<S, 2>(a.W) >= 4 && a.D <= 2);
+    return two && bulk_stages<S, 2>(a.W) >= 2 ? go_bulk<S, NS, SIN, ND, AP, 2>(a, st)
+                                               : go_bulk<S, NS, SIN, ND, AP, 1>(a, st);
 }
 
 }  // namespace

@@ -36,6 +36,8 @@
 //     stores (see fan_out).
 //   * Every staged or loaded 16-byte block holds at least one byte of its
 //     source run, so no access leaves the source allocation's pages.
+//   * On a capped grid (fsdp_plan_set_grid_limit) the fused sync takes the
+//     TMA-bulk-fed kernel of fsdp_bulk.cu instead, where its ring fits.
 //
 // Sources, by page title + section:
 //   [OVERLAP] "Hyper通信掩盖方案" (hyper-parallel issue 184), PR #758 write-up
