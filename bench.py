@@ -71,6 +71,8 @@ def parse(argv=None):
                     help="also measure the pipelined backward over LAYERS layers of --pipeline-workload "
                          "(0: skip)")
     ap.add_argument("--pipeline-workload", default="hsdp_2x4_llama")
+    ap.add_argument("--pipeline-large-layers", type=int, default=3,
+                    help="also the fused syncs' pipeline over this many large (2,8) layers (0: skip)")
     return ap.parse_args(argv)
 
 
@@ -382,6 +384,17 @@ def measured_peaks():
     return 6800.0, "fallback (6.8 TB/s)"
 
 
+def kernel_source_hash():
+    """sha256[:16] of the step kernels' source: fsdp_kernels.cu followed by
+    the device helpers it includes (fsdp_device.cuh)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("fsdp_kernels.cu", "fsdp_device.cuh"):
+        h.update(open(os.path.join(ROOT, "hsdp_sharded_parameter_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (same source hash), else None."""
@@ -390,8 +403,7 @@ def ncu_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "hsdp_sharded_parameter_gb300", "csrc", "fsdp_kernels.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = kernel_source_hash()
     for line in open(path):
         parts = line.split()
         if len(parts) == 4 and not line.startswith("#") and parts[0] == h and parts[1] == kernel \
@@ -575,7 +587,10 @@ def run_gpu(args, wl):
 
     pipeline = None
     if want_pipe:
-        pipeline = run_pipeline(args, dev)
+        pipeline = run_pipeline(args, dev, args.pipeline_workload, args.pipeline)
+        if args.pipeline_large_layers > 0 and args.pipeline_workload != "large_hsdp":
+            pipeline["large_hsdp"] = run_pipeline(args, dev, "large_hsdp", args.pipeline_large_layers,
+                                                  ("one_pass", "fused"))
 
     cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -693,7 +708,7 @@ def run_per_workload(args, dev, peak):
     return out
 
 
-def run_pipeline(args, dev):
+def run_pipeline(args, dev, workload, n, modes=("one_pass", "fused", "unfused_4step")):
     """Overlap of the gradient sync with backward compute over a stack of
     layers ("Hyper通信掩盖方案" PR #758 write-up §二.2: the 4-step pipeline):
     the stand-in backward of a layer is bf16 GEMMs (8192^3, cuBLAS) on the
@@ -710,12 +725,12 @@ def run_pipeline(args, dev):
     from hsdp_sharded_parameter_gb300 import workloads as WL
     from hsdp_sharded_parameter_gb300.runtime import BackwardPipeline, HsdpUnit
 
-    wl = WL.WORKLOADS[args.pipeline_workload]
-    n = args.pipeline
+    wl = WL.WORKLOADS[workload]
+    unfused = "unfused_4step" in modes
     units = []
     for i in range(n):
         u = HsdpUnit(C.Plan(wl.d0, wl.inner, wl.rank_size, wl.shard_size).upload(), wl.param_dtype,
-                     wl.grad_dtype, device=dev, with_unfused=True)
+                     wl.grad_dtype, device=dev, with_unfused=unfused, backward_only=True)
         WL.torch_fill_(u.grads, wl.seed_grads + 100 * i, wl.grad_std, wl.grad_dtype)
         units.append(u)
     a = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
@@ -752,7 +767,8 @@ def run_pipeline(args, dev):
     syncs = {"one_pass": lambda L: units[L].reduce_grads_one_pass("avg"),
              "fused": lambda L: units[L].reduce_grads("avg"),
              "unfused_4step": lambda L: units[L].reduce_grads_unfused("avg")}
-    for mode, sync in syncs.items():
+    for mode in modes:
+        sync = syncs[mode]
         fused, one = mode != "unfused_4step", mode == "one_pass"
         t_sync = timed(lambda: [sync(L) for L in reversed(range(n))])
         res = {"sync_only_ms": round(t_sync, 3), "serial_ms": round(t_comp + t_sync, 3)}

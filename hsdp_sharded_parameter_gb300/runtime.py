@@ -30,7 +30,10 @@ def _empty(numel, dtype, device, role=None):
 
 class HsdpUnit:
     def __init__(self, plan: C.Plan, param_dt="bf16", grad_dt="bf16", ag_dt=None, device="cuda",
-                 with_unfused=False, alloc=None):
+                 with_unfused=False, alloc=None, backward_only=False):
+        """backward_only: allocate only the gradient sync's buffers (grads,
+        fused regions, shard gradients; the RS input with with_unfused);
+        the forward calls are then unavailable."""
         self.plan = plan
         self.param_dt, self.grad_dt = param_dt, grad_dt
         self.ag_dt = ag_dt or param_dt
@@ -40,15 +43,22 @@ class HsdpUnit:
         sl_ag = plan.slice_numel(self.ag_dt)
         sl_f = plan.slice_numel("f32")
         dev = self.device
-        self.shards = [alloc(plan.shard_numel(p, w % S), param_dt, dev, "shards") for w in range(W) for p in range(P)]
-        self.ag_out = [alloc(S * sl_ag, self.ag_dt, dev, "ag_output") for _ in range(W)]
-        self.full = [alloc(plan.numel(p), self.ag_dt, dev, "full_params") for _ in range(W) for p in range(P)]
+        self.backward_only = bool(backward_only)
+        if self.backward_only:
+            self.shards, self.ag_out, self.full = [], [], []
+        else:
+            self.shards = [alloc(plan.shard_numel(p, w % S), param_dt, dev, "shards") for w in range(W)
+                           for p in range(P)]
+            self.ag_out = [alloc(S * sl_ag, self.ag_dt, dev, "ag_output") for _ in range(W)]
+            self.full = [alloc(plan.numel(p), self.ag_dt, dev, "full_params") for _ in range(W) for p in range(P)]
         self.grads = [alloc(plan.numel(p), grad_dt, dev, "grads") for _ in range(W) for p in range(P)]
         self.fused = [alloc(sl_f, "f32", dev, "fused") for _ in range(W)]
         self.shard_grads = [alloc(plan.shard_numel(p, w % S), grad_dt, dev, "shard_grads") for w in range(W) for p in range(P)]
-        self.b_shards = plan.bind("shards", param_dt, self.shards)
-        self.b_ag = plan.bind("ag_output", self.ag_dt, self.ag_out)
-        self.b_full = plan.bind("full_params", self.ag_dt, self.full)
+        self.b_shards = self.b_ag = self.b_full = None
+        if not self.backward_only:
+            self.b_shards = plan.bind("shards", param_dt, self.shards)
+            self.b_ag = plan.bind("ag_output", self.ag_dt, self.ag_out)
+            self.b_full = plan.bind("full_params", self.ag_dt, self.full)
         self.b_grads = plan.bind("grads", grad_dt, self.grads)
         self.b_fused = plan.bind("fused", "f32", self.fused)
         self.b_shard_grads = plan.bind("shard_grads", grad_dt, self.shard_grads)
@@ -135,7 +145,8 @@ class HsdpUnit:
 
     def close(self):
         for b in [self.b_shards, self.b_ag, self.b_full, self.b_grads, self.b_fused, self.b_shard_grads]:
-            b.close()
+            if b is not None:
+                b.close()
         if self.rs_in is not None:
             self.b_rs_in.close()
 
