@@ -520,6 +520,8 @@ __global__ void __launch_bounds__(bulk_threads<G>(), 1) rs_ar_reduce_bulk_kernel
     }
 }
 
+// SM count of the current device, cached per device (the same query as the
+// step kernels' launcher makes; kept here so this file stands alone).
 int bulk_sm_count() {
     static std::mutex mu;
     static std::unordered_map<int, int> cache;

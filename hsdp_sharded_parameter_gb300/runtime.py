@@ -278,6 +278,14 @@ class BackwardPipeline:
             self._apply(L, comp)
         return comp.record_event()
 
+    def check_status(self):
+        """Reads (and clears) every layer's plan status word after the sync
+        has finished; raises if a wait inside a capped-grid sync kernel ran
+        out (its layer's results are then undefined)."""
+        bad = {L: st for L, st in ((L, u.plan.status()) for L, u in enumerate(self.units)) if st}
+        if bad:
+            raise RuntimeError(f"gradient sync: a wait inside the kernel ran out (layer: status bits) {bad}")
+
     @staticmethod
     def finish(event, timeout_s=60.0, poll_s=0.001):
         """Waits on the host for `event` for at most timeout_s seconds;

@@ -227,8 +227,12 @@ int main(void) {
     }
 
     /* the sync in one pass: the same fused regions and shard gradients from
-     * one kernel, on buffers dirtied first */
-    for (int op = FSDP_AVG; op <= FSDP_SUM; ++op) {
+     * one kernel, on buffers dirtied first; the last round on a grid capped
+     * at 3 blocks (the bulk-fed kernel, whose waits report through the
+     * plan's status word) */
+    for (int round = 0; round < 3; ++round) {
+        const int op = round == 1 ? FSDP_SUM : FSDP_AVG;
+        OK(fsdp_plan_set_grid_limit(plan, round == 2 ? 3 : 0));
         for (int w = 0; w < W; ++w) CUDA(cudaMemset(fused[w], 0xFF, (size_t)n_fused[w] * 4));
         for (int i = 0; i < W * P; ++i)
             if (n_shard[i]) CUDA(cudaMemset(sgrad[i], 0xFF, (size_t)n_shard[i] * 2));
@@ -262,7 +266,11 @@ int main(void) {
             }
             free(h);
         }
+        int status = -1;
+        OK(fsdp_plan_status(plan, NULL, &status));
+        CHECK(status == 0, "plan status %d after the one-pass sync (round %d)", status, round);
     }
+    OK(fsdp_plan_set_grid_limit(plan, 0));
 
     OK(fsdp_binding_destroy(b_shards));
     OK(fsdp_binding_destroy(b_ag));

@@ -84,6 +84,24 @@ def test_errors_are_reported_not_crashed():
     assert rc == C.FSDP_ERR_INVALID_ARG
 
 
+def test_wait_limit_and_status_calls_check_their_arguments():
+    # the failure-detection calls of the capped sync: settable on a host-only
+    # plan; reading the status word needs the uploaded plan (it lives in the
+    # plan's device memory) and refuses a NULL output
+    cp = C.Plan([7], [8], 4, 4)
+    assert cp.set_wait_limit(5_000_000) is cp
+    assert cp.set_wait_limit(0) is cp  # 0 restores the default
+    assert cp.inject_stall(True) is cp and cp.inject_stall(False) is cp
+    lib = C.lib()
+    st = ctypes.c_int(-1)
+    rc = lib.fsdp_plan_status(cp.handle, None, ctypes.byref(st))
+    assert rc == C.FSDP_ERR_INVALID_ARG and b"not uploaded" in lib.fsdp_last_error()
+    assert st.value == -1
+    for fn, arg in [(lib.fsdp_plan_set_wait_limit, 1), (lib.fsdp_plan_inject_stall, 1)]:
+        assert fn(None, arg) == C.FSDP_ERR_INVALID_ARG
+    assert lib.fsdp_plan_status(None, None, ctypes.byref(st)) == C.FSDP_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
 def test_upload_without_gpu_fails_cleanly():
     cp = C.Plan([7], [8], 4, 4)

@@ -74,6 +74,7 @@ def test_pipelined_backward_matches_oracle(fused, op, comm_blocks):
     pipe = BackwardPipeline(units, op=op, fused=fused, comm_blocks=comm_blocks, one_pass=one_pass)
     done = pipe.run(backward_compute)
     BackwardPipeline.finish(done, timeout_s=60)
+    pipe.check_status()
     for L, u in enumerate(units):
         exp = oracle_shard_grads(LAYERS[L], truth[L], op, fused)
         for i, (s, e) in enumerate(zip(u.shard_grads, exp)):
