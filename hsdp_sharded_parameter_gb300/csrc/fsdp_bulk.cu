@@ -15,16 +15,21 @@
 //     one 2048-element warp tile of a run); per chunk each of its lanes
 //     announces and issues one `cp.async.bulk` global -> shared copy, of its
 //     own source, completing on the stage's mbarrier (transaction bytes);
-//   * eight consumer warps wait for the stage, fold one 8-element granule
-//     per thread straight from shared memory and store the fp32 sums (and
-//     the applied, rounded shard gradients) from registers, then release
-//     the stage to the producer through a second mbarrier.
+//   * one or two groups of eight consumer warps wait for the stage, fold
+//     one 8-element granule per thread straight from shared memory into
+//     registers, release the stage to the producer through a second
+//     mbarrier, then store the fp32 sums (and the applied, rounded shard
+//     gradients) from registers; a chunk's record (pointers, shifts) lives
+//     in a ring of its own, so it outlasts the data slot.
 // The shared memory holds as many stages as fit (3 for 16 bf16 sources, 6
-// for 8), so up to ~190 KB per SM stay in flight without registers. On one
-// GB300, with 8 bf16 sources into 2 fp32 destinations, contiguous, a probe
-// of this layout measured ~97 GB/s per SM with the copies issued by 8 lanes
-// (64 SMs: 6.3 TB/s), against ~60 GB/s per SM with one issuing thread and
-// 52-67 GB/s per SM for the per-warp cp.async rings.
+// for 8), so up to ~200 KB per SM stay in flight without registers. On one
+// GB300, a probe of this layout (8 bf16 sources into 2 fp32 destinations,
+// contiguous, nothing but the fold) measured ~90-97 GB/s per SM with the
+// copies issued by 8 lanes, against ~60 GB/s per SM with one issuing thread
+// and ~61 GB/s per SM with cp.async from the producer warp; this kernel
+// moves ~76 GB/s per SM with 8 sources and ~92 with 16 (64 SMs: 0.72 and
+// 0.87 of the measured copy peak), against ~30-67 for per-warp cp.async
+// rings.
 //
 // Every wait is bounded: a wait that runs past KArgs::wait_ns sets a bit in
 // the plan's status word (fsdp_plan_status reads it), raises the block's
@@ -67,8 +72,8 @@ constexpr int kBulkMaxStages = 12;
 constexpr int kBulkMaxSources = 32;  // one issuing lane per source
 constexpr int kBulkMaxDests = 32;    // one lane per replica
 
-// What the producer tells the consumers about one stage.
-struct alignas(16) BulkStage {
+// What the producer tells the consumers about one chunk.
+struct alignas(16) ChunkRecord {
     int64_t t;     // the chunk (checked by the consumers before they store)
     int64_t n;     // elements of the run
     int64_t rel0;  // run-relative element of thread 0's first granule (< 0 by the destination's phase)
@@ -93,7 +98,7 @@ __host__ __device__ constexpr size_t bulk_slot() {
 // consumer loop).
 template <typename S>
 __host__ __device__ constexpr int bulk_stages_fit(int ns) {
-    return (int)((kBulkSmem - 2 * sizeof(BulkStage)) / ((size_t)ns * bulk_slot<S>() + sizeof(BulkStage) + 16));
+    return (int)((kBulkSmem - 2 * sizeof(ChunkRecord)) / ((size_t)ns * bulk_slot<S>() + sizeof(ChunkRecord) + 16));
 }
 // As many stages as fit (at most kBulkMaxStages), a multiple of the number
 // of consumer groups G: stage s then always serves group s % G, so a group
@@ -107,7 +112,7 @@ __host__ __device__ constexpr int bulk_stages(int ns) {
 }
 template <typename S>
 __host__ __device__ constexpr size_t bulk_smem(int ns, int nst) {
-    return (size_t)nst * ((size_t)ns * bulk_slot<S>() + 16) + (size_t)(nst + 2) * sizeof(BulkStage);
+    return (size_t)nst * ((size_t)ns * bulk_slot<S>() + 16) + (size_t)(nst + 2) * sizeof(ChunkRecord);
 }
 
 // --------------------------------------------------------------- mbarriers
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(bulk_threads<G>(), 1) rs_ar_reduce_bulk_kernel
     constexpr size_t kSlot = bulk_slot<S>();
     char* ring = smem;
     // chunk q's record is records[q % (nst + 2)]
-    BulkStage* records = reinterpret_cast<BulkStage*>(smem + (size_t)nst * ns * kSlot);
+    ChunkRecord* records = reinterpret_cast<ChunkRecord*>(smem + (size_t)nst * ns * kSlot);
     uint64_t* full = reinterpret_cast<uint64_t*>(records + nst + 2);
     uint64_t* empty = full + nst;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(bulk_threads<G>(), 1) rs_ar_reduce_bulk_kernel
                 if (lane == 0) fail(a, kStatusProducerWait, abort);
                 break;
             }
-            BulkStage& m = records[rec];
+            ChunkRecord& m = records[rec];
             if (++rec == nst + 2) rec = 0;
             if (lane < ns) m.shift[lane] = (int32_t)shift;
             if (lane < nd) {
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(bulk_threads<G>(), 1) rs_ar_reduce_bulk_kernel
             if (lane == 0) fail(a, kStatusConsumerWait, abort);
             break;
         }
-        const BulkStage& m = records[rec];
+        const ChunkRecord& m = records[rec];
         if ((rec += G) >= nst + 2) rec -= nst + 2;
         if (m.t != t) {
             // not this chunk's record: stop before storing anything
