@@ -32,7 +32,8 @@ LAYERS = [([300, 64, 7], [128, 1, 33], 8, 4),
 def build_stack():
     units, truth = [], []
     for i, (d0, inner, W, S) in enumerate(LAYERS):
-        u = HsdpUnit(C.Plan(d0, inner, W, S).upload(), "bf16", "bf16", with_unfused=True)
+        # only the sync's buffers (no forward buffers), as the benchmark's stacks
+        u = HsdpUnit(C.Plan(d0, inner, W, S).upload(), "bf16", "bf16", with_unfused=True, backward_only=True)
         WL.torch_fill_(u.grads, 50 + i, 1.0, "bf16")
         truth.append([g.clone() for g in u.grads])
         units.append(u)
