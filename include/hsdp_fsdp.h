@@ -40,6 +40,10 @@
  *     its one-pass kernel enqueues the two it stands for) and return;
  *     launch failures come back as FSDP_ERR_CUDA. Calls on different streams are safe when the buffers
  *     they write are disjoint from the buffers the others touch.
+ *   - Waits: no kernel waits on another kernel or on the host. The one
+ *     kernel that waits inside (the fused sync on a capped grid, between
+ *     its own warps) bounds every wait and reports one that ran out through
+ *     the plan's status word (fsdp_plan_status), not the return value.
  *   - Pointers: device pointers aligned to their element size; NULL only
  *     for a buffer of 0 elements. 16-byte-aligned pointers (every PyTorch
  *     allocation) take the vectorised path; others take an element-wise
