@@ -216,3 +216,14 @@ def test_grid_limits_give_the_same_bytes(case, cap):
     plan, L, unit, alloc = make(S, D, d0, inner, "bf16", "bf16")
     plan.set_grid_limit(cap)
     check_every_step(L, unit, alloc, seed=10 * cap + len(case), ops=("avg",))
+
+
+@pytest.mark.parametrize("offsets", [None, {"shard_grads": 2, "fused": 4}])
+@pytest.mark.parametrize("S,D", [(4, 2), (8, 1)])
+def test_shifted_apply_plans(S, D, offsets):
+    # a one-element first parameter moves every later o_p off the 16-byte
+    # grid of the fp32 fused rows, so almost all of the apply's data is
+    # shifted (the apply's realigning path, and with unaligned buffers its
+    # element-wise path); every byte against the oracle
+    plan, L, unit, alloc = make(S, D, [1, 3000, 777, 5, 2049], [1, 33, 8, 1, 16], "bf16", "bf16", offsets=offsets)
+    check_every_step(L, unit, alloc, seed=S * 10 + D, ops=("avg", "sum"))
