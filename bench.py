@@ -783,6 +783,9 @@ def run_pipeline(args, dev, workload, n, modes=("one_pass", "fused", "unfused_4s
             row["hidden_frac"] = round((t_comp + t_sync - t_pipe) / max(1e-9, min(t_comp, t_sync)), 3)
             res[f"cap_{cap}"] = row
         out[mode] = res
+    # per schedule: the cap that hid the most of the shorter of compute and sync
+    out["best"] = {m: max(((c, r["hidden_frac"]) for c, r in out[m].items() if c.startswith("cap_")),
+                          key=lambda x: x[1]) for m in modes}
     status = [u.plan.status() for u in units]
     out["status_words"] = status
     for u in units:
