@@ -78,6 +78,21 @@ def test_one_pass_sync_full_size(key):
     free(unit, plan)
 
 
+@pytest.mark.parametrize("key,cap", [("hsdp_2x4_llama", 56), ("large_hsdp", 48), ("ragged_fsdp", 64)])
+def test_capped_one_pass_sync_full_size(key, cap):
+    # the gradient sync as the benchmark's pipeline runs it beside backward
+    # compute: on a grid capped at `cap` blocks (the TMA-bulk-fed kernel),
+    # every byte of the fused regions and shard gradients against the oracle
+    wl, plan, L, unit = build(key)
+    plan.set_grid_limit(cap)
+    unit.reduce_grads_one_pass("avg")
+    torch.cuda.synchronize()
+    plan.set_grid_limit(0)
+    assert plan.status() == 0
+    FP.check_unit(L, unit, "avg", forward=False)
+    free(unit, plan)
+
+
 def test_pure_tp_sum_op():
     # the DTensor-managed (pure TP) default is SUM ("Hyper通信掩盖方案" PR #758 §二.3)
     wl, plan, L, unit = build("pure_tp_compat")
