@@ -581,13 +581,17 @@ cudaError_t go_bulk_shape(const KArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+bool bulk_reduce_fits(int sdt, int W, int D) {
+    if (W > kBulkMaxSources || D > kBulkMaxDests) return false;
+    if (sdt == FSDP_F32) return bulk_stages<float, 1>(W) >= 2;
+    if (sdt == FSDP_BF16) return bulk_stages<uint16_t, 1>(W) >= 2;
+    return false;
+}
+
 cudaError_t launch_bulk_reduce(int sdt, const KArgs& a, cudaStream_t st, bool* used) {
     *used = false;
     const bool sf = sdt == FSDP_F32;
-    if (!a.status || a.max_grid <= 0 || a.reps != 1 || a.W > kBulkMaxSources || a.D > kBulkMaxDests ||
-        (sdt != FSDP_F32 && sdt != FSDP_BF16))
-        return cudaSuccess;
-    if ((sf ? bulk_stages<float, 1>(a.W) : bulk_stages<uint16_t, 1>(a.W)) < 2) return cudaSuccess;
+    if (!a.status || a.max_grid <= 0 || a.reps != 1 || !bulk_reduce_fits(sdt, a.W, a.D)) return cudaSuccess;
     *used = true;
     const bool ap = a.sg_tab != nullptr;
     if (sf) return ap ? go_bulk_shape<float, 0, 0, 0, true>(a, st) : go_bulk_shape<float, 0, 0, 0, false>(a, st);

@@ -502,6 +502,10 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
         pl->tables[t].ntiles = tiles[t].back();
     }
     pl->device = dev;
+    if (cudaDeviceGetAttribute(&pl->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        pl->sm_count = 0;
+    }
     pl->uploaded = true;
     return FSDP_OK;
 }
@@ -888,6 +892,14 @@ int fsdp_rs_ar_reduce_apply(fsdp_plan_t pl, fsdp_binding_t grads, fsdp_binding_t
     // the fused buffer keeps the raw sum; the shard gradients divide by W
     // for AVG, as fsdp_apply_grads does [OVERLAP PR #758 §二.3]
     set_divisor(a, op == FSDP_AVG ? pl->W : 1);
+    // Sources mostly shifted against the fused rows (staged_blocks 3, the
+    // ragged layer): the TMA-bulk-fed kernel on every SM (one block per SM)
+    // measured faster than the staged one there (0.868 -> 0.967 of the
+    // measured copy peak on one GB300) and slower on unshifted layers (HSDP
+    // (2,4) 1.027 -> 0.927, pure-TP 0.957 -> 0.858), which keep it.
+    if (a.max_grid == 0 && pl->staged_blocks == 3 && pl->sm_count > 0 &&
+        bulk_reduce_fits(grads->dt, pl->W, pl->D))
+        a.max_grid = pl->sm_count;
     return run(K_RSAR, grads->dt, FSDP_F32, a, stream, "rs_ar_reduce_apply");
 }
 

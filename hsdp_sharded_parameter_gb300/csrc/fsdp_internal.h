@@ -149,6 +149,9 @@ bool can_fold_apply(int src_dt, int W, int D);
 // false, launching nothing, when the shape does not fit its shared-memory
 // ring (the caller then takes the staged kernels).
 cudaError_t launch_bulk_reduce(int src_dt, const KArgs& a, cudaStream_t stream, bool* used);
+// Whether that kernel's shared-memory ring fits W sources of this dtype
+// (and D replicas).
+bool bulk_reduce_fits(int src_dt, int W, int D);
 
 // Status bits a kernel with internal waits sets in the plan's status word.
 constexpr int kStatusProducerWait = 1;  // a stage was not released in time
@@ -167,6 +170,7 @@ struct fsdp_plan_s {
     uint64_t wait_ns = 1000000000ull;  // fsdp_plan_set_wait_limit
     int stall = 0;                     // fsdp_plan_inject_stall
     int* dev_status = nullptr;         // inside dev_block
+    int sm_count = 0;                  // of the plan's device, set by fsdp_plan_upload
     int staged_blocks = 2;  // see KArgs::staged_blocks, set by fsdp_plan_upload
     bool agout_shifted = false;  // see KArgs::shifted (bf16 copy-out), set by fsdp_plan_upload
     void* dev_block = nullptr;

@@ -41,9 +41,10 @@
  *     launch failures come back as FSDP_ERR_CUDA. Calls on different streams are safe when the buffers
  *     they write are disjoint from the buffers the others touch.
  *   - Waits: no kernel waits on another kernel or on the host. The one
- *     kernel that waits inside (the fused sync on a capped grid, between
- *     its own warps) bounds every wait and reports one that ran out through
- *     the plan's status word (fsdp_plan_status), not the return value.
+ *     kernel that waits inside (the fused sync on a capped grid, and the
+ *     one-pass sync of a mostly shifted plan; between its own warps) bounds
+ *     every wait and reports one that ran out through the plan's status
+ *     word (fsdp_plan_status), not the return value.
  *   - Pointers: device pointers aligned to their element size; NULL only
  *     for a buffer of 0 elements. 16-byte-aligned pointers (every PyTorch
  *     allocation) take the vectorised path; others take an element-wise
@@ -335,7 +336,11 @@ int fsdp_ar_reduce(fsdp_plan_t plan, fsdp_binding_t fused, int op, fsdp_stream_t
  * No counterpart as one call in the pages (which apply after the fused
  * AllReduce). shard_grads must have the gradient dtype. One kernel when the
  * staged reduce fits the mesh (up to 32 bf16 or ~26 fp32 sources);
- * otherwise the two calls it stands for, in order on `stream`. */
+ * otherwise the two calls it stands for, in order on `stream`. When most of
+ * the plan's gradient runs are shifted against the fused rows' 16-byte grid
+ * (a ragged layout) and no grid cap is set, the kernel is the TMA-bulk-fed
+ * one on every SM (as under a cap; its waits report through
+ * fsdp_plan_status). */
 int fsdp_rs_ar_reduce_apply(fsdp_plan_t plan, fsdp_binding_t grads, fsdp_binding_t fused, int op,
                             int accumulate, fsdp_binding_t shard_grads, fsdp_stream_t stream);
 
