@@ -500,6 +500,12 @@ int fsdp_plan_upload(fsdp_plan_t pl) {
             mapped[t] ? reinterpret_cast<const int32_t*>(static_cast<char*>(block) + run_at[t]) : nullptr;
         pl->tables[t].nseg = (int)segs[t].size();
         pl->tables[t].ntiles = tiles[t].back();
+        if (t == T_AGIN_BF16 || t == T_AGOUT_BF16) {
+            bool any = false;
+            for (const Seg& g : segs[t])
+                if (g.p >= 0 && (((g.src_off - g.dst_off) * 2) & 15) != 0) any = true;
+            pl->tables[t].any_shifted = any;
+        }
     }
     pl->device = dev;
     if (cudaDeviceGetAttribute(&pl->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -767,6 +773,8 @@ int fsdp_ag_copy_in(fsdp_plan_t pl, fsdp_binding_t shards, fsdp_binding_t ag_out
     a.dst_tab = ag_out->dev_table;
     a.fuse = fuse_gather ? 1 : 0;
     a.vec = ag_out->aligned16;
+    a.aligned_runs = !pl->tables[ag_out->dt == FSDP_F32 ? T_AGIN_F32 : T_AGIN_BF16].any_shifted &&
+                     shards->aligned16 && ag_out->aligned16;
     return run(K_AGIN, shards->dt, ag_out->dt, a, stream, "ag_copy_in");
 }
 
@@ -797,6 +805,8 @@ int fsdp_ag_copy_out(fsdp_plan_t pl, fsdp_binding_t ag_out, fsdp_binding_t full,
     a.dst_tab = full->dev_table;
     a.vec = full->aligned16;
     a.shifted = pl->agout_shifted ? 1 : 0;
+    a.aligned_runs = !pl->tables[full->dt == FSDP_F32 ? T_AGOUT_F32 : T_AGOUT_BF16].any_shifted &&
+                     ag_out->aligned16 && full->aligned16;
     return run(K_AGOUT, ag_out->dt, full->dt, a, stream, "ag_copy_out");
 }
 

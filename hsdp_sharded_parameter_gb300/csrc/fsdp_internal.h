@@ -66,6 +66,9 @@ struct Table {
     const int32_t* tile_run = nullptr;   // device, ntiles: the run of each tile
     int nseg = 0;
     int64_t ntiles = 0;
+    // some data run's source is off its destination's 16-byte phase (with
+    // 16-byte aligned buffers): the copies then need their realigning path
+    bool any_shifted = true;
 };
 
 inline int elem_size(int dt) { return dt == FSDP_F32 ? 4 : (dt == FSDP_BF16 ? 2 : 0); }
@@ -104,6 +107,11 @@ struct KArgs {
     // the destination's 16-byte grid (copy-out picks its grid by it).
     int shifted;
     int dests;  // destinations written per tile when more than one (the gather)
+    // Copies: no run's source is shifted against its destination and both
+    // bindings are 16-byte aligned, so the kernel without the realigning
+    // path (fewer registers, more resident warps) may run (it still routes
+    // any shifted tile through its per-granule path).
+    int aligned_runs;
     // The fused reduce with the apply folded in: the [W][P] table of
     // actual-shard gradients it also writes (nullptr: not folded in).
     void* const* sg_tab;
