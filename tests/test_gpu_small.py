@@ -95,6 +95,18 @@ def test_unaligned_pointers(offsets):
     check_every_step(L, unit, alloc, seed=3)
 
 
+@pytest.mark.parametrize("S,D", [(4, 2), (8, 1), (2, 4)])
+@pytest.mark.parametrize("offsets", [None, {"shards": 16, "ag_output": 16, "full_params": 16}, {"shards": 2}])
+def test_plans_with_no_shifted_run(S, D, offsets):
+    # every inner size a multiple of 8 elements puts every run's source on
+    # its destination's 16-byte phase: with 16-byte aligned buffers the bf16
+    # copy-in and copy-out take their build without the realigning path
+    # (uneven dim 0: padding rows, ragged tails, runs over many tiles); a
+    # shard buffer 2 bytes off the grid sends them back to the general build
+    plan, L, unit, alloc = make(S, D, [1000, 7, 3, 513, 64], [8, 24, 16, 8, 40], "bf16", "bf16", offsets=offsets)
+    check_every_step(L, unit, alloc, seed=S * 10 + D)
+
+
 @pytest.mark.parametrize("dts", [("bf16", "bf16", "bf16"), ("f32", "f32", "f32"), ("f32", "bf16", "bf16")])
 def test_special_values(dts):
     # subnormals (kept: no flush to zero), signed zeros, overflow to infinity,
